@@ -1,0 +1,299 @@
+"""Pins for the FP64 oracle against things other than itself (CPU only).
+
+Each check is chosen so that a plausible slip in the oracle (a wrong GQA head
+map, a dropped 1/sqrt(D), an off-by-one causal bound, a transposed operand, a
+wrong page index) fails at least one of them:
+
+* a library special case: torch float64 ``scaled_dot_product_attention`` with
+  ``enable_gqa`` (its K/V heads are repeat-interleaved, i.e. q head h uses kv
+  head h // (H_q/H_kv) = floor(h*H_kv/H_q));
+* closed forms: identical V rows, identical K rows (mean of the allowed V
+  rows), causal row 0, zero keys (lse = ln n), a one-hot query against a
+  large-margin key;
+* invariants: paged == contiguous, decode == last prefill row, block-table
+  permutation, splitting the keys and merging by lse.
+
+Sources of the definitions: "Tutorial: Adding a New Kernel to RL.cu"
+(add-cuda-kernel page), include/kernels/attention.cuh and
+tests/test_attention.cu (reference attention, scale 1/sqrt(D), causal j <= i,
+GQA map, paged layout); the Kimi-K2.6 KernelBench trace for the online-softmax
+identity that the lse merge relies on.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+import workloads as W
+
+
+def _rand16(rng, shape, scale=1.0):
+    return (rng.standard_normal(shape) * scale).astype(np.float16)
+
+
+def _sdpa(Q, K, V, causal):
+    # [B,S,H,D] -> [B,H,S,D], float64 on CPU
+    q = torch.from_numpy(Q.astype(np.float64)).permute(0, 2, 1, 3)
+    k = torch.from_numpy(K.astype(np.float64)).permute(0, 2, 1, 3)
+    v = torch.from_numpy(V.astype(np.float64)).permute(0, 2, 1, 3)
+    o = F.scaled_dot_product_attention(q, k, v, is_causal=causal, enable_gqa=True)
+    return o.permute(0, 2, 1, 3).numpy()
+
+
+def test_half_decode_all_patterns():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.half_to_double(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+SHAPES = [  # (B, S, H_q, H_kv, D)
+    (1, 16, 2, 1, 128),   # first prefill case of the page's test file
+    (2, 7, 4, 2, 4),
+    (1, 9, 6, 3, 8),
+    (1, 5, 4, 4, 16),     # H_kv == H_q (MHA)
+    (2, 11, 8, 2, 32),    # 4:1 groups
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("causal", [True, False])
+def test_prefill_matches_torch_sdpa_float64(shape, causal):
+    B, S, H_q, H_kv, D = shape
+    rng = np.random.default_rng(1234 + S)
+    Q, K, V = _rand16(rng, (B, S, H_q, D)), _rand16(rng, (B, S, H_kv, D)), _rand16(rng, (B, S, H_kv, D))
+    O = oracle.prefill(Q, K, V, causal=causal)
+    ref = _sdpa(Q, K, V, causal)
+    np.testing.assert_allclose(O, ref, rtol=0, atol=1e-12)
+
+
+def test_prefill_gqa_map_distinguishes_groups():
+    # each kv head's V is a constant vector equal to its index: O row = g(h)
+    B, S, H_q, H_kv, D = 1, 6, 8, 2, 4
+    rng = np.random.default_rng(7)
+    Q, K = _rand16(rng, (B, S, H_q, D)), _rand16(rng, (B, S, H_kv, D))
+    V = np.zeros((B, S, H_kv, D), np.float16)
+    for g in range(H_kv):
+        V[:, :, g, :] = g + 1
+    O = oracle.prefill(Q, K, V, causal=True)
+    for h in range(H_q):
+        np.testing.assert_allclose(O[:, :, h, :], (h * H_kv) // H_q + 1, rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_identical_v_rows_give_that_row(causal):
+    B, S, H_q, H_kv, D = 2, 13, 4, 2, 16
+    rng = np.random.default_rng(3)
+    Q, K = _rand16(rng, (B, S, H_q, D), 2.0), _rand16(rng, (B, S, H_kv, D), 2.0)
+    row = _rand16(rng, (B, 1, H_kv, D))
+    V = np.broadcast_to(row, (B, S, H_kv, D)).copy()
+    O = oracle.prefill(Q, K, V, causal=causal)
+    g = (np.arange(H_q) * H_kv) // H_q
+    expect = np.broadcast_to(row[:, :, g, :].astype(np.float64), O.shape)
+    np.testing.assert_allclose(O, expect, rtol=1e-14, atol=1e-14)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_identical_k_rows_give_mean_of_allowed_v(causal):
+    B, S, H_q, H_kv, D = 1, 12, 4, 2, 8
+    rng = np.random.default_rng(4)
+    Q = _rand16(rng, (B, S, H_q, D))
+    krow = _rand16(rng, (B, 1, H_kv, D))
+    K = np.broadcast_to(krow, (B, S, H_kv, D)).copy()
+    V = _rand16(rng, (B, S, H_kv, D))
+    O, lse = oracle.prefill(Q, K, V, causal=causal, with_lse=True)
+    Vd = V.astype(np.float64)
+    for h in range(H_q):
+        g = h * H_kv // H_q
+        for i in range(S):
+            n = i + 1 if causal else S
+            np.testing.assert_allclose(O[0, i, h], Vd[0, :n, g].mean(axis=0), atol=1e-14)
+            s = float(np.dot(Q[0, i, h].astype(np.float64), krow[0, 0, g].astype(np.float64))) / math.sqrt(D)
+            assert abs(lse[0, i, h] - (s + math.log(n))) < 1e-12
+
+
+def test_causal_row0_is_v0_and_zero_keys_lse():
+    B, S, H_q, H_kv, D = 2, 9, 4, 1, 128
+    rng = np.random.default_rng(5)
+    Q, K, V = _rand16(rng, (B, S, H_q, D), 3.0), _rand16(rng, (B, S, H_kv, D), 3.0), _rand16(rng, (B, S, H_kv, D))
+    O = oracle.prefill(Q, K, V, causal=True)
+    for h in range(H_q):
+        assert np.array_equal(O[:, 0, h], V[:, 0, 0].astype(np.float64))
+    Kz = np.zeros_like(K)
+    _, lse = oracle.prefill(Q, Kz, V, causal=True, with_lse=True)
+    np.testing.assert_allclose(lse[0, :, 0], np.log(np.arange(1, S + 1)), atol=1e-14)
+    _, lse = oracle.prefill(Q, Kz, V, causal=False, with_lse=True)
+    np.testing.assert_allclose(lse, math.log(S), atol=1e-14)
+
+
+def test_one_hot_query_selects_large_margin_key():
+    # q = c*e_0, key j* has k[0] = 1 and the others 0: weight of j* is
+    # 1 / (1 + (n-1) e^{-c/sqrt(D)}); with c/sqrt(D) = 64 it is 1 to 1e-27.
+    B, S, H_q, H_kv, D = 1, 8, 2, 1, 4
+    Q = np.zeros((B, S, H_q, D), np.float16)
+    Q[..., 0] = 128.0
+    K = np.zeros((B, S, H_kv, D), np.float16)
+    K[0, 3, 0, 0] = 1.0
+    rng = np.random.default_rng(6)
+    V = _rand16(rng, (B, S, H_kv, D))
+    O = oracle.prefill(Q, K, V, causal=False)
+    np.testing.assert_allclose(O[0, :, 0], np.broadcast_to(V[0, 3, 0].astype(np.float64), (S, D)), atol=1e-20)
+    # causal rows before the key cannot see it: uniform mean over their prefix
+    O = oracle.prefill(Q, K, V, causal=True)
+    np.testing.assert_allclose(O[0, 2, 1], V[0, :3, 0].astype(np.float64).mean(0), atol=1e-15)
+
+
+def test_mha_heads_independent():
+    B, S, H, D = 1, 10, 3, 16
+    rng = np.random.default_rng(8)
+    Q, K, V = _rand16(rng, (B, S, H, D)), _rand16(rng, (B, S, H, D)), _rand16(rng, (B, S, H, D))
+    O = oracle.prefill(Q, K, V)
+    for h in range(H):
+        Oh = oracle.prefill(Q[:, :, h:h + 1].copy(), K[:, :, h:h + 1].copy(), V[:, :, h:h + 1].copy())
+        assert np.array_equal(O[:, :, h:h + 1], Oh)
+
+
+def test_prefill_rows_equal_full():
+    B, S, H_q, H_kv, D = 2, 20, 4, 2, 32
+    rng = np.random.default_rng(9)
+    Q, K, V = _rand16(rng, (B, S, H_q, D)), _rand16(rng, (B, S, H_kv, D)), _rand16(rng, (B, S, H_kv, D))
+    for causal in (True, False):
+        O, lse = oracle.prefill(Q, K, V, causal=causal, with_lse=True)
+        rows = [(1, 19, 3), (0, 0, 0), (1, 7, 2), (0, 13, 1)]
+        Or, lr = oracle.prefill_rows(Q, K, V, rows, causal=causal, with_lse=True)
+        for r, (b, i, h) in enumerate(rows):
+            assert np.array_equal(Or[r], O[b, i, h]) and lr[r] == lse[b, i, h]
+
+
+# ------------------------------------------------------------------ decode
+
+def _page(K, bs, perm):
+    """Contiguous per-sequence K [N, L, H_kv, D] -> paged cache via perm of pages."""
+    N, L, H_kv, D = K.shape
+    npg = (L + bs - 1) // bs
+    cache = np.full((N * npg, H_kv, bs, D), np.nan, np.float16)
+    table = np.full((N, npg + 2), -1, np.int32)
+    for n in range(N):
+        for p in range(npg):
+            phys = int(perm[n * npg + p])
+            table[n, p] = phys
+            t0, t1 = p * bs, min(L, (p + 1) * bs)
+            cache[phys, :, : t1 - t0, :] = K[n, t0:t1].transpose(1, 0, 2)
+    return cache, table
+
+
+@pytest.mark.parametrize("bs", [16, 5])
+def test_decode_paged_equals_last_prefill_row(bs):
+    B, S, H_q, H_kv, D = 3, 37, 4, 2, 16
+    rng = np.random.default_rng(10)
+    Q, K, V = _rand16(rng, (B, S, H_q, D)), _rand16(rng, (B, S, H_kv, D)), _rand16(rng, (B, S, H_kv, D))
+    O = oracle.prefill(Q, K, V, causal=True)
+    perm = rng.permutation(B * ((S + bs - 1) // bs)).astype(np.int32)
+    kc, table = _page(K, bs, perm)
+    vc, _ = _page(V, bs, perm)
+    out = oracle.decode_paged(Q[:, S - 1].copy(), kc, vc, table, np.full(B, S, np.int32))
+    np.testing.assert_allclose(out, O[:, S - 1], rtol=0, atol=1e-14)
+    # unused (NaN-poisoned) slots of the last page were never read
+    assert np.isfinite(out).all()
+
+
+def test_decode_matches_sdpa_on_gathered_keys_ragged():
+    N, H_q, H_kv, D, bs = 4, 8, 2, 32, 16
+    rng = np.random.default_rng(11)
+    lens = np.array([1, 16, 17, 50], np.int32)
+    tables, nb = W.decode_layout(lens, bs, 5, seed=3)
+    kc, vc = _rand16(rng, (nb, H_kv, bs, D)), _rand16(rng, (nb, H_kv, bs, D))
+    q = _rand16(rng, (N, H_q, D))
+    out = oracle.decode_paged(q, kc, vc, tables, lens)
+    for n in range(N):
+        L = int(lens[n])
+        t = np.arange(L)
+        kk = kc[tables[n, t // bs], :, t % bs, :]  # [L, H_kv, D]
+        vv = vc[tables[n, t // bs], :, t % bs, :]
+        ref = _sdpa(q[n][None, None], kk[None], vv[None], causal=False)[0, 0]
+        np.testing.assert_allclose(out[n], ref, atol=1e-12)
+
+
+def test_decode_empty_sequence_gives_zero_and_neg_inf_lse():
+    N, H_q, H_kv, D, bs = 2, 2, 1, 8, 16
+    rng = np.random.default_rng(12)
+    lens = np.array([0, 3], np.int32)
+    tables = np.array([[-1], [0]], np.int32)
+    kc, vc = _rand16(rng, (1, H_kv, bs, D)), _rand16(rng, (1, H_kv, bs, D))
+    out, lse = oracle.decode_paged(_rand16(rng, (N, H_q, D)), kc, vc, tables, lens, with_lse=True)
+    assert np.all(out[0] == 0) and np.all(lse[0] == -np.inf)
+    assert np.all(np.isfinite(lse[1]))
+
+
+def test_decode_block_permutation_invariant_and_rows():
+    cfg = W.DecodeConfig("t", 5, 4, 2, D=16, block_size=4, len_lo=1, len_hi=30, max_blocks_per_seq=8)
+    inp = W.decode_inputs(cfg, seed=2)
+    out = oracle.decode_paged(inp.q, inp.k_cache, inp.v_cache, inp.block_tables, inp.seq_lens)
+    # move every physical block to a new place and rewrite the tables to match
+    nb = inp.num_blocks
+    p = np.random.default_rng(13).permutation(nb).astype(np.int32)
+    kc2 = np.empty_like(inp.k_cache)
+    vc2 = np.empty_like(inp.v_cache)
+    kc2[p] = inp.k_cache
+    vc2[p] = inp.v_cache
+    bt2 = np.where(inp.block_tables >= 0, p[np.maximum(inp.block_tables, 0)], -1).astype(np.int32)
+    out2 = oracle.decode_paged(inp.q, kc2, vc2, bt2, inp.seq_lens)
+    assert np.array_equal(out, out2)
+    rows = [(4, 3), (0, 0), (2, 1)]
+    orow = oracle.decode_paged_rows(inp.q, inp.k_cache, inp.v_cache, inp.block_tables, inp.seq_lens, rows)
+    for r, (n, h) in enumerate(rows):
+        assert np.array_equal(orow[r], out[n, h])
+
+
+# ----------------------------------------------------------------- combine
+
+def _segment_partials(q, Kseq, Vseq, cuts):
+    """Oracle decode over each key segment [cuts[i], cuts[i+1]) of one sequence,
+    each laid out as its own single-sequence paged problem (block size 1)."""
+    H_q, D = q.shape
+    H_kv = Kseq.shape[1]
+    O_part, lse_part = [], []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        L = b - a
+        kc = Kseq[a:b][:, :, None, :].copy() if L else np.zeros((1, H_kv, 1, D), np.float16)
+        vc = Vseq[a:b][:, :, None, :].copy() if L else np.zeros((1, H_kv, 1, D), np.float16)
+        table = np.arange(max(L, 1), dtype=np.int32)[None]
+        o, l = oracle.decode_paged(q[None], kc, vc, table, np.array([L], np.int32), with_lse=True)
+        O_part.append(o[0])
+        lse_part.append(l[0])
+    return np.stack(O_part, 1), np.stack(lse_part, 1)  # [H_q, n_split, D], [H_q, n_split]
+
+
+@pytest.mark.parametrize("cuts", [[0, 40], [0, 17, 40], [0, 1, 2, 33, 40], [0, 0, 13, 13, 40, 40]])
+def test_lse_merge_of_segments_equals_whole(cuts):
+    H_q, H_kv, D, L = 4, 2, 16, 40
+    rng = np.random.default_rng(14)
+    q = _rand16(rng, (H_q, D), 2.0)
+    Kseq, Vseq = _rand16(rng, (L, H_kv, D), 2.0), _rand16(rng, (L, H_kv, D))
+    O_part, lse_part = _segment_partials(q, Kseq, Vseq, cuts)
+    out, lse = oracle.lse_combine(O_part, lse_part, with_lse=True)
+    full, lfull = oracle.decode_paged(q[None], Kseq[:, :, None, :].copy(), Vseq[:, :, None, :].copy(),
+                                      np.arange(L, dtype=np.int32)[None], np.array([L], np.int32),
+                                      with_lse=True)
+    np.testing.assert_allclose(out, full[0], atol=1e-13)
+    np.testing.assert_allclose(lse, lfull[0], atol=1e-12)
+
+
+def test_lse_merge_all_empty():
+    out, lse = oracle.lse_combine(np.ones((2, 3, 4)), np.full((2, 3), -np.inf), with_lse=True)
+    assert np.all(out == 0) and np.all(lse == -np.inf)
+
+
+def test_lse_merge_two_known_partials():
+    # two singleton segments with scores a, b: weights e^a/(e^a+e^b), e^b/(e^a+e^b)
+    a, b = 0.3, -1.1
+    O_part = np.array([[[1.0, 0.0], [0.0, 1.0]]])
+    out, lse = oracle.lse_combine(O_part, np.array([[a, b]]), with_lse=True)
+    wa = math.exp(a) / (math.exp(a) + math.exp(b))
+    np.testing.assert_allclose(out[0], [wa, 1 - wa], atol=1e-15)
+    assert abs(lse[0] - math.log(math.exp(a) + math.exp(b))) < 1e-15
