@@ -1,0 +1,179 @@
+"""ctypes binding of libattn_gb300 (the C ABI declared in include/attn.h).
+
+Argument marshalling only: tensors are checked for device, dtype and layout,
+turned into raw pointers, and passed with the current CUDA stream.  Every
+computation runs in the library's CUDA kernels.  There is no fallback: if the
+library cannot be built or loaded, or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+import torch
+
+from . import build as _build
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = -1
+ATTN_ERR_UNSUPPORTED = -2
+ATTN_ERR_CUDA = -3
+ATTN_ERR_TIMEOUT = -4
+ATTN_ERR_BAD_INPUT = -5
+ATTN_ERR_WORKSPACE = -6
+
+EXPORTED = [
+    "attn_prefill", "attn_decode_paged", "attn_decode_paged_workspace_bytes",
+    "attn_decode_paged_ws", "attn_lse_combine", "attn_release_workspace",
+    "attn_get_device_error", "attn_last_cuda_error", "attn_status_string", "attn_version",
+]
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = f"{where}: {status_string(status)} ({status})"
+        if status == ATTN_ERR_CUDA and _lib is not None:
+            msg += f", cudaError {_lib.attn_last_cuda_error()}"
+        super().__init__(msg)
+
+
+def load():
+    """Build (if stale) and load libattn_gb300.so; returns the ctypes handle."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            lib = ctypes.CDLL(path)
+            p, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+            lib.attn_prefill.argtypes = [p, p, p, p, i, i, i, i, i, i, p]
+            lib.attn_decode_paged.argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, p]
+            lib.attn_decode_paged_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
+            lib.attn_decode_paged_workspace_bytes.restype = sz
+            lib.attn_decode_paged_ws.argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, i, p, sz, p]
+            lib.attn_lse_combine.argtypes = [p, p, p, i, i, i, p]
+            lib.attn_release_workspace.argtypes = []
+            lib.attn_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_int), i]
+            lib.attn_last_cuda_error.argtypes = []
+            lib.attn_status_string.argtypes = [i]
+            lib.attn_status_string.restype = ctypes.c_char_p
+            lib.attn_version.argtypes = []
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load().attn_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != ATTN_OK:
+        raise AttnError(status, where)
+
+
+def _stream(stream, device) -> int:
+    if stream is None:
+        return torch.cuda.current_stream(device).cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtype: torch.dtype):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def attn_prefill(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.Tensor,
+                 causal: bool = True, stream=None) -> None:
+    """O <- attention(Q, K, V) for [B,S,H,128] FP16 tensors (GQA, causal or full)."""
+    if Q.dim() != 4 or K.dim() != 4 or V.shape != K.shape or O.shape != Q.shape:
+        raise ValueError("expected Q,O [B,S,H_q,D] and K,V [B,S,H_kv,D]")
+    B, S, H_q, D = Q.shape
+    if K.shape[0] != B or K.shape[1] != S or K.shape[3] != D:
+        raise ValueError("K/V batch, sequence and head_dim must match Q")
+    args = [_dev(Q, "Q", torch.float16), _dev(K, "K", torch.float16),
+            _dev(V, "V", torch.float16), _dev(O, "O", torch.float16)]
+    st = _stream(stream, Q.device)
+    _check(load().attn_prefill(*args, B, S, H_q, K.shape[2], D, int(bool(causal)),
+                               ctypes.c_void_p(st)), "attn_prefill")
+
+
+def _decode_args(q, k_cache, v_cache, out, block_tables, seq_lens):
+    if q.dim() != 3 or k_cache.dim() != 4 or v_cache.shape != k_cache.shape or out.shape != q.shape:
+        raise ValueError("expected q,out [N,H_q,D] and caches [num_blocks,H_kv,block_size,D]")
+    N, H_q, D = q.shape
+    if block_tables.dim() != 2 or block_tables.shape[0] != N or seq_lens.shape != (N,):
+        raise ValueError("expected block_tables [N,max_blocks_per_seq] and seq_lens [N]")
+    ptrs = [_dev(q, "q", torch.float16), _dev(k_cache, "k_cache", torch.float16),
+            _dev(v_cache, "v_cache", torch.float16), _dev(out, "out", torch.float16),
+            _dev(block_tables, "block_tables", torch.int32), _dev(seq_lens, "seq_lens", torch.int32)]
+    sizes = [N, H_q, k_cache.shape[1], D, block_tables.shape[1], k_cache.shape[2]]
+    return ptrs, sizes
+
+
+def attn_decode_paged(q, k_cache, v_cache, out, block_tables, seq_lens, stream=None) -> None:
+    """out <- single-token attention of q over the paged cache (library-owned scratch)."""
+    ptrs, sizes = _decode_args(q, k_cache, v_cache, out, block_tables, seq_lens)
+    st = _stream(stream, q.device)
+    _check(load().attn_decode_paged(*ptrs, *sizes, ctypes.c_void_p(st)), "attn_decode_paged")
+
+
+def attn_decode_paged_workspace_bytes(num_seqs: int, H_q: int, H_kv: int, D: int,
+                                      max_blocks_per_seq: int, block_size: int,
+                                      pages_per_split: int = 0) -> int:
+    return int(load().attn_decode_paged_workspace_bytes(num_seqs, H_q, H_kv, D,
+                                                        max_blocks_per_seq, block_size,
+                                                        pages_per_split))
+
+
+def attn_decode_paged_ws(q, k_cache, v_cache, out, block_tables, seq_lens,
+                         workspace: torch.Tensor, pages_per_split: int = 0, stream=None) -> None:
+    """attn_decode_paged with a caller-owned scratch tensor (any dtype, contiguous, on device)."""
+    ptrs, sizes = _decode_args(q, k_cache, v_cache, out, block_tables, seq_lens)
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    nbytes = workspace.numel() * workspace.element_size()
+    st = _stream(stream, q.device)
+    _check(load().attn_decode_paged_ws(*ptrs, *sizes, int(pages_per_split),
+                                       ctypes.c_void_p(workspace.data_ptr()), nbytes,
+                                       ctypes.c_void_p(st)), "attn_decode_paged_ws")
+
+
+def attn_lse_combine(O_part: torch.Tensor, lse: torch.Tensor, out: torch.Tensor,
+                     stream=None) -> None:
+    """out[r] <- merge of O_part[r, i] weighted by exp(lse[r, i]) (FP32 in, FP16 out)."""
+    if O_part.dim() != 3 or lse.shape != O_part.shape[:2] or out.shape != (O_part.shape[0], O_part.shape[2]):
+        raise ValueError("expected O_part [R,n_split,D], lse [R,n_split], out [R,D]")
+    R, n_split, D = O_part.shape
+    ptrs = [_dev(O_part, "O_part", torch.float32), _dev(lse, "lse", torch.float32),
+            _dev(out, "out", torch.float16)]
+    st = _stream(stream, O_part.device)
+    _check(load().attn_lse_combine(*ptrs, R, n_split, D, ctypes.c_void_p(st)), "attn_lse_combine")
+
+
+def attn_release_workspace() -> None:
+    _check(load().attn_release_workspace(), "attn_release_workspace")
+
+
+def attn_get_device_error(reset: bool = True) -> int:
+    """Raw device error bits of the current device (synchronises); 0 when clean."""
+    code = ctypes.c_int(0)
+    st = load().attn_get_device_error(ctypes.byref(code), int(bool(reset)))
+    if st not in (ATTN_OK, ATTN_ERR_TIMEOUT, ATTN_ERR_BAD_INPUT):
+        raise AttnError(st, "attn_get_device_error")
+    return code.value
+
+
+def attn_version() -> int:
+    return int(load().attn_version())

@@ -1,0 +1,241 @@
+// api.cu -- the C ABI of libattn_gb300: argument validation, workspace
+// ownership, error mapping.  Every compute step runs in the kernels of
+// prefill.cu and decode.cu.
+#include <cstdint>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include <cuda_runtime.h>
+
+#include "attn.h"
+#include "internal.h"
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e)
+{
+    t_last_cuda_error = static_cast<int>(e);
+    return ATTN_ERR_CUDA;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb)
+{
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+int check_heads(int H_q, int H_kv)
+{
+    if (H_q < 1 || H_kv < 1 || H_q % H_kv != 0)
+        return ATTN_ERR_INVALID_ARG;
+    return ATTN_OK;
+}
+
+// Library-owned split-K scratch: one grow-only buffer per (device, stream).
+struct Workspace {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+};
+std::mutex g_ws_mutex;
+std::map<std::pair<int, uintptr_t>, Workspace> g_ws;
+
+int get_workspace(size_t need, cudaStream_t stream, void** out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    Workspace& w = g_ws[{dev, reinterpret_cast<uintptr_t>(stream)}];
+    if (w.bytes < need) {
+        if (w.ptr) {
+            e = cudaFree(w.ptr);  // synchronous: earlier kernels using it have finished
+            w.ptr = nullptr;
+            w.bytes = 0;
+            if (e != cudaSuccess)
+                return cuda_fail(e);
+        }
+        const size_t grow = need + need / 4;
+        e = cudaMalloc(&w.ptr, grow);
+        if (e != cudaSuccess) {
+            w.ptr = nullptr;
+            return cuda_fail(e);
+        }
+        w.bytes = grow;
+    }
+    *out = w.ptr;
+    return ATTN_OK;
+}
+
+int validate_decode(const void* q, const void* k_cache, const void* v_cache, void* out,
+                    const int* block_tables, const int* seq_lens, int num_seqs, int H_q, int H_kv,
+                    int D, int max_blocks_per_seq, int block_size)
+{
+    if (num_seqs < 0 || max_blocks_per_seq < 1 || check_heads(H_q, H_kv) != ATTN_OK)
+        return ATTN_ERR_INVALID_ARG;
+    if (D != attn::kHeadDim || block_size != attn::kPageSize)
+        return ATTN_ERR_UNSUPPORTED;
+    if (num_seqs == 0)
+        return ATTN_OK;
+    if (!q || !k_cache || !v_cache || !out || !block_tables || !seq_lens)
+        return ATTN_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+        !aligned(block_tables, 4) || !aligned(seq_lens, 4))
+        return ATTN_ERR_INVALID_ARG;
+    const size_t qbytes = (size_t)num_seqs * H_q * D * 2;
+    if (overlap(out, qbytes, q, qbytes))
+        return ATTN_ERR_INVALID_ARG;
+    return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ATTN_API int attn_prefill(const void* Q, const void* K, const void* V, void* O, int B, int S,
+                          int H_q, int H_kv, int D, int causal, cudaStream_t stream)
+{
+    if (B < 0 || S < 0 || check_heads(H_q, H_kv) != ATTN_OK)
+        return ATTN_ERR_INVALID_ARG;
+    if (D != attn::kHeadDim)
+        return ATTN_ERR_UNSUPPORTED;
+    if (B == 0 || S == 0)
+        return ATTN_OK;
+    if (!Q || !K || !V || !O)
+        return ATTN_ERR_INVALID_ARG;
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16))
+        return ATTN_ERR_INVALID_ARG;
+    const size_t qbytes = (size_t)B * S * H_q * D * 2;
+    const size_t kvbytes = (size_t)B * S * H_kv * D * 2;
+    if (overlap(O, qbytes, Q, qbytes) || overlap(O, qbytes, K, kvbytes) ||
+        overlap(O, qbytes, V, kvbytes))
+        return ATTN_ERR_INVALID_ARG;
+    const cudaError_t e = attn::launch_prefill(Q, K, V, O, B, S, H_q, H_kv, causal, stream);
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+ATTN_API size_t attn_decode_paged_workspace_bytes(int num_seqs, int H_q, int H_kv, int D,
+                                                  int max_blocks_per_seq, int block_size,
+                                                  int pages_per_split)
+{
+    if (num_seqs < 0 || max_blocks_per_seq < 1 || check_heads(H_q, H_kv) != ATTN_OK ||
+        D != attn::kHeadDim || block_size != attn::kPageSize)
+        return 0;
+    return attn::decode_workspace_bytes(
+        attn::make_decode_plan(num_seqs, H_q, H_kv, max_blocks_per_seq, pages_per_split));
+}
+
+ATTN_API int attn_decode_paged_ws(const void* q, const void* k_cache, const void* v_cache,
+                                  void* out, const int* block_tables, const int* seq_lens,
+                                  int num_seqs, int H_q, int H_kv, int D, int max_blocks_per_seq,
+                                  int block_size, int pages_per_split, void* workspace,
+                                  size_t workspace_bytes, cudaStream_t stream)
+{
+    const int v = validate_decode(q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q,
+                                  H_kv, D, max_blocks_per_seq, block_size);
+    if (v != ATTN_OK || num_seqs == 0)
+        return v;
+    const attn::DecodePlan p =
+        attn::make_decode_plan(num_seqs, H_q, H_kv, max_blocks_per_seq, pages_per_split);
+    if (!workspace || !aligned(workspace, 256) ||
+        workspace_bytes < attn::decode_workspace_bytes(p))
+        return ATTN_ERR_WORKSPACE;
+    const cudaError_t e = attn::launch_decode(p, q, k_cache, v_cache, out, block_tables, seq_lens,
+                                              workspace, stream);
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+ATTN_API int attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
+                               void* out, const int* block_tables, const int* seq_lens,
+                               int num_seqs, int H_q, int H_kv, int D, int max_blocks_per_seq,
+                               int block_size, cudaStream_t stream)
+{
+    const int v = validate_decode(q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q,
+                                  H_kv, D, max_blocks_per_seq, block_size);
+    if (v != ATTN_OK || num_seqs == 0)
+        return v;
+    const attn::DecodePlan p = attn::make_decode_plan(num_seqs, H_q, H_kv, max_blocks_per_seq, 0);
+    void* ws = nullptr;
+    const size_t need = attn::decode_workspace_bytes(p);
+    const int r = get_workspace(need, stream, &ws);
+    if (r != ATTN_OK)
+        return r;
+    const cudaError_t e =
+        attn::launch_decode(p, q, k_cache, v_cache, out, block_tables, seq_lens, ws, stream);
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+ATTN_API int attn_lse_combine(const float* O_part, const float* lse, void* out, int R,
+                              int n_split, int D, cudaStream_t stream)
+{
+    if (R < 0 || n_split < 1)
+        return ATTN_ERR_INVALID_ARG;
+    if (D != attn::kHeadDim)
+        return ATTN_ERR_UNSUPPORTED;
+    if (R == 0)
+        return ATTN_OK;
+    if (!O_part || !lse || !out || !aligned(O_part, 16) || !aligned(lse, 4) || !aligned(out, 16))
+        return ATTN_ERR_INVALID_ARG;
+    const cudaError_t e = attn::launch_lse_combine(O_part, lse, out, R, n_split, stream);
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+ATTN_API int attn_release_workspace(void)
+{
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    int prev = 0;
+    cudaError_t first = cudaGetDevice(&prev);
+    for (auto& kv : g_ws) {
+        if (kv.second.ptr) {
+            cudaError_t e = cudaSetDevice(kv.first.first);
+            if (e == cudaSuccess)
+                e = cudaFree(kv.second.ptr);
+            if (e != cudaSuccess && first == cudaSuccess)
+                first = e;
+        }
+    }
+    g_ws.clear();
+    cudaSetDevice(prev);
+    return first == cudaSuccess ? ATTN_OK : cuda_fail(first);
+}
+
+ATTN_API int attn_get_device_error(int* code, int reset)
+{
+    if (!code)
+        return ATTN_ERR_INVALID_ARG;
+    int v = 0;
+    const cudaError_t e = attn::read_device_error(&v, reset != 0);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    *code = v;
+    if (v & attn::kDevErrTimeout)
+        return ATTN_ERR_TIMEOUT;
+    if (v)
+        return ATTN_ERR_BAD_INPUT;
+    return ATTN_OK;
+}
+
+ATTN_API int attn_last_cuda_error(void) { return t_last_cuda_error; }
+
+ATTN_API const char* attn_status_string(int status)
+{
+    switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported size (head_dim must be 128, block_size 16)";
+    case ATTN_ERR_CUDA: return "CUDA runtime error";
+    case ATTN_ERR_TIMEOUT: return "a bounded device wait timed out";
+    case ATTN_ERR_BAD_INPUT: return "bad block table or sequence length seen on the device";
+    case ATTN_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+    }
+}
+
+ATTN_API int attn_version(void) { return 100; }
+
+}  // extern "C"

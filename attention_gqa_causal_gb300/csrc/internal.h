@@ -1,0 +1,54 @@
+// internal.h -- declarations shared by the translation units of libattn_gb300.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace attn {
+
+constexpr int kHeadDim = 128;   // the only head_dim the kernels are built for
+constexpr int kPageSize = 16;   // the only KV block size the kernels are built for
+
+// Device error word bits (set by kernels, read by attn_get_device_error).
+enum DeviceError : int {
+    kDevErrTimeout = 1,        // a bounded mbarrier wait gave up
+    kDevErrBadBlockId = 2,     // a block_tables entry < 0 inside a sequence's range
+    kDevErrSeqTooLong = 4,     // seq_lens[n] > max_blocks_per_seq * block_size
+    kDevErrTmemAlloc = 8,      // TMEM base address outside the expected range
+};
+
+// Set by the kernels (atomicOr); defined in decode.cu.  Device address of the
+// word on the current device, or nullptr on failure.
+int* device_error_word();
+// Copy the word of the current device to *out (synchronous); optionally clear it.
+cudaError_t read_device_error(int* out, bool reset);
+
+struct DecodePlan {
+    int num_seqs, H_q, H_kv, max_blocks_per_seq;
+    int group;           // H_q / H_kv
+    int heads_per_cta;   // query heads one CTA processes against each loaded KV page
+    int chunks;          // ceil(group / heads_per_cta)
+    int pages_per_split; // KV pages per split (one CTA each)
+    int n_split;         // ceil(max_blocks_per_seq / pages_per_split)
+    size_t o_part_bytes, lse_part_bytes;
+};
+
+DecodePlan make_decode_plan(int num_seqs, int H_q, int H_kv, int max_blocks_per_seq,
+                            int pages_per_split);
+size_t decode_workspace_bytes(const DecodePlan& p);
+
+// Launch split-K main kernel + combine.  `ws` holds at least decode_workspace_bytes(p).
+cudaError_t launch_decode(const DecodePlan& p, const void* q, const void* k_cache,
+                          const void* v_cache, void* out, const int* block_tables,
+                          const int* seq_lens, void* ws, cudaStream_t stream);
+
+// Merge R rows of n_split partials (O normalised per split, lse natural log).
+cudaError_t launch_lse_combine(const float* O_part, const float* lse_part, void* out, int R,
+                               int n_split, cudaStream_t stream);
+
+// Prefill: O = softmax(Q K^T / sqrt(D), causal) V over [B,S,H,D] tensors.
+cudaError_t launch_prefill(const void* Q, const void* K, const void* V, void* O, int B, int S,
+                           int H_q, int H_kv, int causal, cudaStream_t stream);
+
+}  // namespace attn

@@ -1,0 +1,504 @@
+// prefill.cu -- causal / full grouped-query attention prefill on sm_103a
+// tensor cores (tcgen05 + TMEM + TMA).
+//
+// Operation ("Tutorial: Adding a New Kernel to RL.cu", add-cuda-kernel page,
+// include/kernels/attention.cuh, "Flash Attention 2 -- Prefill"): Q,O are
+// [B,S,H_q,D], K,V are [B,S,H_kv,D], FP16 in and out with FP32 accumulation;
+// q head h reads kv head h*H_kv/H_q; with the causal mask token i attends to
+// positions <= i; scale 1/sqrt(D).  The online-softmax recurrence (running
+// max m, rescale factor exp(m_old - m_new), running sum l, final O/l) is the
+// one the same page's kernel walks per key and the "GRPO-CUDA Project Memory"
+// page summarises under "Attention kernel design"; here it runs per 128-key
+// tile on tensor-core scores.
+//
+// GB300 design (one CTA per SM, 320 threads):
+//   warps 0-3  softmax warpgroup 0  (Q tile 0, TMEM lanes 0..127 = its rows)
+//   warps 4-7  softmax warpgroup 1  (Q tile 1)
+//   warp  8    MMA issuer (one lane) + TMEM allocation
+//   warp  9    TMA producer (one lane)
+// A CTA owns two 128-row Q tiles that read the same K/V: two query heads of
+// one GQA group over the same rows when the group size is even (identical
+// causal extents), else two consecutive row tiles of one head.  Per 128-key
+// tile j the MMA warp computes S_t = Q_t K_j^T into TMEM (FP32), softmax
+// warpgroup t turns its row of S_t into P_t = exp2(S*c - m) and writes P_t
+// back over S_t in TMEM as FP16, and the MMA warp accumulates
+// O_t += P_t V_j with A read from TMEM.  The two tiles ping-pong: while one
+// warpgroup runs its softmax the tensor core works on the other tile.
+// TMEM: S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512) columns.
+// SMEM: Q0,Q1 (32 KB each), 2 K stages, 2 V stages (32 KB each), all
+// 128-byte swizzled as written by TMA boxes of 64 x 128.
+// The running max is rescaled lazily: O and l are rescaled only when the row
+// max grows by more than kRescaleThreshold (log2 units), which keeps the
+// result exact (m, l and O always refer to the same reference max) while
+// making the TMEM read-modify-write of O rare.  Key tiles wholly above the
+// diagonal are never loaded or multiplied; only the diagonal tile is masked.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int BM = 128;  // query rows per tile
+constexpr int BN = 128;  // keys per tile
+constexpr int D = kHeadDim;
+constexpr int kThreads = 320;
+constexpr int kStages = 2;
+constexpr uint32_t kTileBytes = BM * D * 2;      // 32 KB
+constexpr uint32_t kBoxBytes = kTileBytes / 2;   // 16 KB: 128 rows x 64 halves
+constexpr uint32_t kSmemQ = 0;
+constexpr uint32_t kSmemK = 2 * kTileBytes;
+constexpr uint32_t kSmemV = kSmemK + kStages * kTileBytes;
+constexpr uint32_t kSmemBytes = kSmemV + kStages * kTileBytes;
+constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;  // slack for 1024-byte alignment
+constexpr float kRescaleThreshold = 8.0f;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct PrefillArgs {
+    __half* O;
+    int* err;
+    int B, S, H_q, H_kv;
+    int group;          // H_q / H_kv
+    int head_pairs;     // 1: the two tiles are two heads; 0: two row tiles of one head
+    int units_per_mb;   // B * H_kv * (tile pairs per kv head)
+    int n_mb;           // number of row blocks
+    int causal;
+    float scale_log2;   // log2(e) / sqrt(D)
+};
+
+struct Unit {
+    int b, g, head[2], row0[2], n_kv;
+};
+
+__device__ __forceinline__ Unit decode_unit(const PrefillArgs& a, int u)
+{
+    Unit w;
+    // causal: longest row blocks first so short ones fill the tail of the grid
+    const int mb = a.causal ? a.n_mb - 1 - u / a.units_per_mb : u / a.units_per_mb;
+    int r = u % a.units_per_mb;
+    const int per_g = a.units_per_mb / (a.B * a.H_kv);
+    const int pr = r % per_g;
+    r /= per_g;
+    w.g = r % a.H_kv;
+    w.b = r / a.H_kv;
+    if (a.head_pairs) {
+        w.head[0] = w.g * a.group + 2 * pr;
+        w.head[1] = w.head[0] + 1;
+        w.row0[0] = w.row0[1] = mb * BM;
+    } else {
+        w.head[0] = w.head[1] = w.g * a.group + pr;
+        w.row0[0] = mb * 2 * BM;
+        w.row0[1] = w.row0[0] + BM;
+    }
+    const int last_row = min(a.S - 1, w.row0[1] + BM - 1);
+    w.n_kv = a.causal ? last_row / BN + 1 : (a.S + BN - 1) / BN;
+    return w;
+}
+
+struct SmemCtl {
+    uint64_t q_full;
+    uint64_t k_full[kStages], k_empty[kStages];
+    uint64_t v_full[kStages], v_empty[kStages];
+    uint64_t s_full[2], p_full[2], o_full[2];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int abort;
+};
+
+__device__ __forceinline__ void flag_abort(SmemCtl* c, int* err)
+{
+    c->abort = 1;
+    atomicOr(err, kDevErrTimeout);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, const PrefillArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ SmemCtl ctl;
+    const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const Unit w = decode_unit(a, blockIdx.x);
+    volatile int* abort = &ctl.abort;
+
+    if (threadIdx.x == 0) {
+        ctl.abort = 0;
+        mbar_init(smem_u32(&ctl.q_full), 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&ctl.k_full[s]), 1);
+            mbar_init(smem_u32(&ctl.k_empty[s]), 1);
+            mbar_init(smem_u32(&ctl.v_full[s]), 1);
+            mbar_init(smem_u32(&ctl.v_empty[s]), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(smem_u32(&ctl.s_full[t]), 1);
+            mbar_init(smem_u32(&ctl.p_full[t]), 128);
+            mbar_init(smem_u32(&ctl.o_full[t]), 1);
+        }
+        mbar_init(smem_u32(&ctl.mma_done), 1);
+        fence_mbar_init();
+    }
+    if (warp == 8) {
+        tmem_alloc(smem_u32(&ctl.tmem_base), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl.tmem_base;
+
+    if (warp == 9) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            const uint32_t qbar = smem_u32(&ctl.q_full);
+            mbar_arrive_expect_tx(qbar, 2 * kTileBytes);
+            for (int t = 0; t < 2; ++t)
+                for (int h = 0; h < 2; ++h)
+                    tma_load_4d(sbase + kSmemQ + t * kTileBytes + h * kBoxBytes, &tmQ, qbar, h * 64,
+                                w.head[t], w.row0[t], w.b);
+            int n_k = 0, n_v = 0;  // K / V tiles issued so far
+            bool ok = true;
+            for (int j = 0; j < w.n_kv && ok; ++j) {
+                const int s = j % kStages;
+                const uint32_t ph = (j / kStages) & 1;
+                ok = mbar_wait(smem_u32(&ctl.k_empty[s]), ph ^ 1, abort);
+                if (!ok)
+                    break;
+                const uint32_t kbar = smem_u32(&ctl.k_full[s]);
+                mbar_arrive_expect_tx(kbar, kTileBytes);
+                for (int h = 0; h < 2; ++h)
+                    tma_load_4d(sbase + kSmemK + s * kTileBytes + h * kBoxBytes, &tmK, kbar, h * 64,
+                                w.g, j * BN, w.b);
+                ++n_k;
+                ok = mbar_wait(smem_u32(&ctl.v_empty[s]), ph ^ 1, abort);
+                if (!ok)
+                    break;
+                const uint32_t vbar = smem_u32(&ctl.v_full[s]);
+                mbar_arrive_expect_tx(vbar, kTileBytes);
+                for (int h = 0; h < 2; ++h)
+                    tma_load_4d(sbase + kSmemV + s * kTileBytes + h * kBoxBytes, &tmV, vbar, h * 64,
+                                w.g, j * BN, w.b);
+                ++n_v;
+            }
+            if (!ok)
+                flag_abort(&ctl, a.err);
+            // drain: every copy this CTA started has landed before shared memory
+            // is released (bounded by time only, not by the abort flag)
+            const int no_abort = 0;
+            mbar_wait(qbar, 0, &no_abort);
+            for (int s = 0; s < kStages; ++s) {
+                // loads issued into stage s: tiles j < n with j % kStages == s
+                const int ck = n_k > s ? (n_k - s + kStages - 1) / kStages : 0;
+                const int cv = n_v > s ? (n_v - s + kStages - 1) / kStages : 0;
+                if (ck)
+                    mbar_wait(smem_u32(&ctl.k_full[s]), (ck - 1) & 1, &no_abort);
+                if (cv)
+                    mbar_wait(smem_u32(&ctl.v_full[s]), (cv - 1) & 1, &no_abort);
+            }
+        }
+    } else if (warp == 8) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc_s = idesc_f16_f32(BM, BN, false, false);
+            const uint32_t idesc_o = idesc_f16_f32(BM, D, false, true);
+            auto issue_s = [&](int t, int s) {
+                const uint32_t sK = sbase + kSmemK + s * kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk / 4) * kBoxBytes + (kk % 4) * 32;
+                    mma_f16_ss(tmem + t * BN, sdesc_sw128(sbase + kSmemQ + t * kTileBytes + off, 16, 1024),
+                               sdesc_sw128(sK + off, 16, 1024), idesc_s, kk > 0);
+                }
+            };
+            auto issue_o = [&](int t, int s, bool acc) {
+                const uint32_t sV = sbase + kSmemV + s * kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_f16_ts(tmem + 256 + t * D, tmem + t * BN + kk * 8,
+                               sdesc_sw128(sV + kk * 2048, kBoxBytes, 1024), idesc_o,
+                               (acc || kk > 0) ? 1u : 0u);
+            };
+            bool ok = mbar_wait(smem_u32(&ctl.q_full), 0, abort) &&
+                      mbar_wait(smem_u32(&ctl.k_full[0]), 0, abort);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0, 0);
+                mma_commit(smem_u32(&ctl.s_full[0]));
+                issue_s(1, 0);
+                mma_commit(smem_u32(&ctl.s_full[1]));
+                mma_commit(smem_u32(&ctl.k_empty[0]));
+            }
+            for (int j = 0; j < w.n_kv && ok; ++j) {
+                const int s = j % kStages;
+                const uint32_t ph = (j / kStages) & 1;
+                const int s1 = (j + 1) % kStages;
+                const uint32_t ph1 = ((j + 1) / kStages) & 1;
+                const bool more = j + 1 < w.n_kv;
+                ok = mbar_wait(smem_u32(&ctl.v_full[s]), ph, abort) &&
+                     mbar_wait(smem_u32(&ctl.p_full[0]), j & 1, abort);
+                if (!ok)
+                    break;
+                tc_fence_after();
+                issue_o(0, s, j > 0);
+                if (!more)
+                    mma_commit(smem_u32(&ctl.o_full[0]));
+                if (more) {
+                    ok = mbar_wait(smem_u32(&ctl.k_full[s1]), ph1, abort);
+                    if (!ok)
+                        break;
+                    tc_fence_after();
+                    issue_s(0, s1);
+                    mma_commit(smem_u32(&ctl.s_full[0]));
+                }
+                ok = mbar_wait(smem_u32(&ctl.p_full[1]), j & 1, abort);
+                if (!ok)
+                    break;
+                tc_fence_after();
+                issue_o(1, s, j > 0);
+                mma_commit(smem_u32(&ctl.v_empty[s]));
+                if (!more)
+                    mma_commit(smem_u32(&ctl.o_full[1]));
+                if (more) {
+                    issue_s(1, s1);
+                    mma_commit(smem_u32(&ctl.s_full[1]));
+                    mma_commit(smem_u32(&ctl.k_empty[s1]));
+                }
+            }
+            if (!ok)
+                flag_abort(&ctl, a.err);
+            // drain: all MMAs issued by this thread are complete before TMEM is released
+            const int no_abort = 0;
+            mma_commit(smem_u32(&ctl.mma_done));
+            mbar_wait(smem_u32(&ctl.mma_done), 0, &no_abort);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax warpgroups
+        const int t = warp / 4;
+        const int row = (warp % 4) * 32 + lane;       // row within the tile = TMEM lane
+        const int my_row0 = t ? w.row0[1] : w.row0[0];
+        const int my_head = t ? w.head[1] : w.head[0];
+        const int q_row = my_row0 + row;              // row within the sequence
+        const uint32_t lane_addr = static_cast<uint32_t>((warp % 4) * 32) << 16;
+        const uint32_t tS = tmem + lane_addr + t * BN;
+        const uint32_t tO = tmem + lane_addr + 256 + t * D;
+        const float c = a.scale_log2;
+        float m_ref = -CUDART_INF_F;  // reference max (log2 units) shared by l and O
+        float l_sum = 0.f;
+        bool ok = true;
+        for (int j = 0; j < w.n_kv; ++j) {
+            ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.s_full[t]), j & 1, abort));
+            if (!ok)
+                break;
+            tc_fence_after();
+            uint32_t sr[4][32];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+                tmem_ld32(tS + q4 * 32, sr[q4]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+                reg_fence32(sr[q4]);
+            // mask keys beyond the causal bound / the sequence end
+            const int kv0 = j * BN;
+            const int limit = a.causal ? min(q_row + 1, a.S) - kv0 : a.S - kv0;
+            if (__any_sync(0xffffffffu, limit < BN)) {
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (q4 * 32 + i >= limit)
+                            sr[q4][i] = __float_as_uint(-CUDART_INF_F);
+            }
+            float mx = -CUDART_INF_F;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    mx = fmaxf(mx, __uint_as_float(sr[q4][i]));
+            const float m_new = fmaxf(m_ref, mx * c);
+            const bool grow = m_new > m_ref + kRescaleThreshold;
+            float alpha = 1.f;
+            if (grow) {
+                alpha = ex2_approx(m_ref - m_new);
+                m_ref = m_new;
+                l_sum *= alpha;
+            }
+            // P = exp2(S*c - m_ref), packed in place (pair of columns -> even slot)
+            // and written as FP16 over the first 64 columns of S_t
+            const float neg_m = -m_ref;
+            float rs = 0.f;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    const float p0 = ex2_approx(fmaf(__uint_as_float(sr[q4][i]), c, neg_m));
+                    const float p1 = ex2_approx(fmaf(__uint_as_float(sr[q4][i + 1]), c, neg_m));
+                    rs += p0 + p1;
+                    sr[q4][i] = pack_half2(p0, p1);
+                }
+            }
+            tmem_st32_even(tS, sr[0], sr[1]);
+            tmem_st32_even(tS + 32, sr[2], sr[3]);
+            l_sum += rs;
+            if (j > 0 && __any_sync(0xffffffffu, grow)) {
+                // O_t holds the previous tiles' sum (its last PV completed before
+                // s_full fired and the next PV waits for p_full): bring it to the
+                // new reference max
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint32_t orr[32];
+                    tmem_ld32(tO + q4 * 32, orr);
+                    tmem_ld_wait();
+                    reg_fence32(orr);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+                    tmem_st32(tO + q4 * 32, orr);
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&ctl.p_full[t]));
+        }
+        if (ok)
+            ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.o_full[t]), 0, abort));
+        if (!ok) {
+            flag_abort(&ctl, a.err);
+        } else {
+            tc_fence_after();
+            const float inv = 1.f / l_sum;
+            const bool store = q_row < a.S;
+            __half* dst = a.O + (((size_t)w.b * a.S + q_row) * a.H_q + my_head) * D;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t orr[32];
+                tmem_ld32(tO + q4 * 32, orr);
+                tmem_ld_wait();
+                reg_fence32(orr);
+                if (store) {
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        uint4 pk;
+                        pk.x = pack_half2(__uint_as_float(orr[8 * v + 0]) * inv, __uint_as_float(orr[8 * v + 1]) * inv);
+                        pk.y = pack_half2(__uint_as_float(orr[8 * v + 2]) * inv, __uint_as_float(orr[8 * v + 3]) * inv);
+                        pk.z = pack_half2(__uint_as_float(orr[8 * v + 4]) * inv, __uint_as_float(orr[8 * v + 5]) * inv);
+                        pk.w = pack_half2(__uint_as_float(orr[8 * v + 6]) * inv, __uint_as_float(orr[8 * v + 7]) * inv);
+                        *reinterpret_cast<uint4*>(dst + q4 * 32 + v * 8) = pk;
+                    }
+                }
+            }
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 8)
+        tmem_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// [B,S,H,128] FP16 tensor, boxes of 64 head-dim x 1 head x 128 rows x 1 batch, 128B swizzle.
+bool make_bshd_map(CUtensorMap* m, const void* ptr, int B, int S, int H)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc)
+        return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2,
+                                   (cuuint64_t)S * H * D * 2};
+    const cuuint32_t box[4] = {64, 1, BM, 1};
+    const cuuint32_t es[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(ptr), dims, strides, box,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const void* Q, const void* K, const void* V, void* O, int B, int S,
+                           int H_q, int H_kv, int causal, cudaStream_t stream)
+{
+    // the shared-memory opt-in is a per-device attribute
+    static std::mutex attr_mutex;
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= 64)
+        return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lock(attr_mutex);
+        if (!attr_done[dev]) {
+            e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kSmemAlloc);
+            if (e != cudaSuccess)
+                return e;
+            attr_done[dev] = true;
+        }
+    }
+    CUtensorMap mq, mk, mv;
+    if (!make_bshd_map(&mq, Q, B, S, H_q) || !make_bshd_map(&mk, K, B, S, H_kv) ||
+        !make_bshd_map(&mv, V, B, S, H_kv))
+        return cudaErrorInvalidValue;
+    PrefillArgs a{};
+    a.O = static_cast<__half*>(O);
+    a.err = device_error_word();
+    if (!a.err)
+        return cudaErrorInvalidSymbol;
+    a.B = B;
+    a.S = S;
+    a.H_q = H_q;
+    a.H_kv = H_kv;
+    a.group = H_q / H_kv;
+    a.head_pairs = (a.group % 2 == 0) ? 1 : 0;
+    const int pairs_per_g = a.head_pairs ? a.group / 2 : a.group;
+    a.n_mb = a.head_pairs ? (S + BM - 1) / BM : (S + 2 * BM - 1) / (2 * BM);
+    a.units_per_mb = B * H_kv * pairs_per_g;
+    a.causal = causal ? 1 : 0;
+    a.scale_log2 = kLog2e / sqrtf((float)D);
+    const long long grid = (long long)a.units_per_mb * a.n_mb;
+    if (grid > 0x7fffffffLL)
+        return cudaErrorInvalidConfiguration;
+    prefill_kernel<<<(unsigned)grid, kThreads, kSmemAlloc, stream>>>(mq, mk, mv, a);
+    return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -1,0 +1,148 @@
+/*
+ * attn.h -- C ABI of libattn_gb300: grouped-query attention for one GB300
+ * (sm_103a) GPU.  Plain pointers and sizes only.
+ *
+ * Conventions for every entry point
+ *  - Tensors are caller-owned DEVICE buffers, dense and contiguous in the
+ *    layouts stated below (no stride arguments).  FP16 buffers must be
+ *    16-byte aligned; int32 buffers 4-byte aligned.
+ *  - Calls are asynchronous on `stream` (0 = the legacy default stream of the
+ *    current device) and return once the kernels are launched.  They never
+ *    synchronise the device, never print, never exit.
+ *  - Arguments are validated on the host before anything is launched; on any
+ *    non-zero return nothing was launched (except ATTN_ERR_CUDA from the
+ *    launch itself).
+ *  - Return 0 (ATTN_OK) on success, else a negative ATTN_ERR_* code.
+ *  - Preconditions the host cannot check (the library never reads device
+ *    memory on the host) are listed per call.  The kernels check the cheap
+ *    ones on the device, skip the offending work and record it in the device
+ *    error word (attn_get_device_error).
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = -1,  /* null/misaligned pointer, negative size, H_q % H_kv != 0, O aliasing an input */
+    ATTN_ERR_UNSUPPORTED = -2,  /* head_dim != 128 or block_size != 16 */
+    ATTN_ERR_CUDA = -3,         /* a CUDA runtime call failed; see attn_last_cuda_error() */
+    ATTN_ERR_TIMEOUT = -4,      /* device error word: a bounded on-chip wait gave up */
+    ATTN_ERR_BAD_INPUT = -5,    /* device error word: negative block id or seq_len beyond the table */
+    ATTN_ERR_WORKSPACE = -6     /* caller workspace missing or smaller than required */
+};
+
+/*
+ * Prefill attention.
+ * Operation: "Tutorial: Adding a New Kernel to RL.cu" (add-cuda-kernel page),
+ * include/kernels/attention.cuh, "Flash Attention 2 -- Prefill":
+ *   O[b,i,h,:] = sum_j softmax_j(Q[b,i,h,:].K[b,j,g,:] / sqrt(D)) V[b,j,g,:]
+ *   with g = h*H_kv/H_q, j over 0..i if causal, else over 0..S-1.
+ * Q, O : [B, S, H_q, D] FP16.   K, V : [B, S, H_kv, D] FP16.
+ * D must be 128 (else ATTN_ERR_UNSUPPORTED); H_q % H_kv == 0.
+ * B == 0 or S == 0 is a no-op.  O must not overlap Q, K or V.
+ * Accumulation is FP32; the output is rounded to nearest-even FP16.
+ */
+ATTN_API int attn_prefill(const void* Q, const void* K, const void* V, void* O, int B, int S,
+                          int H_q, int H_kv, int D, int causal, cudaStream_t stream);
+
+/*
+ * Single-token decode over a paged KV cache.
+ * Operation: same page, "Paged Attention -- Decode":
+ *   out[n,h,:] = sum_{t < seq_lens[n]} softmax_t(q[n,h,:].K_t / sqrt(D)) V_t,
+ *   K_t = k_cache[block_tables[n, t/block_size], g, t % block_size, :] (V_t alike),
+ *   g = h*H_kv/H_q.  seq_lens counts the context including the new token.
+ * q, out        : [num_seqs, H_q, D] FP16
+ * k/v_cache     : [num_blocks, H_kv, block_size, D] FP16
+ * block_tables  : [num_seqs, max_blocks_per_seq] int32, logical -> physical block
+ * seq_lens      : [num_seqs] int32
+ * D must be 128 and block_size 16 (else ATTN_ERR_UNSUPPORTED).
+ * A sequence with seq_lens[n] == 0 gets out = 0.  num_seqs == 0 is a no-op.
+ * Only the first ceil(seq_lens[n]/block_size) table entries of a row and the
+ * first seq_lens[n] slots of the context are read; the rest may hold anything.
+ * Device-side preconditions: 0 <= block_tables[n][p] < num_blocks for the
+ * pages in use (negative ids are skipped and flagged; ids >= num_blocks cannot
+ * be detected: there is no num_blocks argument), and
+ * seq_lens[n] <= max_blocks_per_seq*block_size (longer ones are clamped and
+ * flagged).
+ * Scratch for the split-K partials comes from a library-owned grow-only
+ * buffer per (device, stream); growing it calls cudaMalloc/cudaFree (which
+ * synchronise the device).  Use attn_decode_paged_ws to pass your own.
+ */
+ATTN_API int attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
+                               void* out, const int* block_tables, const int* seq_lens,
+                               int num_seqs, int H_q, int H_kv, int D, int max_blocks_per_seq,
+                               int block_size, cudaStream_t stream);
+
+/*
+ * Bytes of scratch attn_decode_paged_ws needs for these sizes.
+ * pages_per_split: KV pages per split-K work unit (<= 0 picks the default, 16).
+ * Returns 0 for invalid sizes.
+ */
+ATTN_API size_t attn_decode_paged_workspace_bytes(int num_seqs, int H_q, int H_kv, int D,
+                                                  int max_blocks_per_seq, int block_size,
+                                                  int pages_per_split);
+
+/*
+ * attn_decode_paged with caller scratch: `workspace` is a device buffer of
+ * at least attn_decode_paged_workspace_bytes(...) bytes, 256-byte aligned,
+ * owned by the caller, and must not be used by another call that overlaps on
+ * the GPU.  The call allocates nothing.  Same semantics otherwise; the result
+ * does not depend on pages_per_split beyond FP32 rounding.
+ */
+ATTN_API int attn_decode_paged_ws(const void* q, const void* k_cache, const void* v_cache,
+                                  void* out, const int* block_tables, const int* seq_lens,
+                                  int num_seqs, int H_q, int H_kv, int D, int max_blocks_per_seq,
+                                  int block_size, int pages_per_split, void* workspace,
+                                  size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Merge partial attention results over disjoint key segments by their
+ * log-sum-exp (the combine step of split-K decode):
+ *   L = log sum_i exp(lse[r,i]),  out[r,:] = sum_i exp(lse[r,i] - L) O_part[r,i,:]
+ * O_part : [R, n_split, D] FP32, each normalised over its segment
+ * lse    : [R, n_split]    FP32 natural log; -inf marks an empty segment
+ * out    : [R, D] FP16 (a row whose segments are all empty gets 0).
+ * D must be 128.  Basis: the online-softmax identity o_N/l_N = sum v e^s / sum e^s
+ * worked through in the Kimi-K2.6 KernelBench trace (fused cross-attention page).
+ */
+ATTN_API int attn_lse_combine(const float* O_part, const float* lse, void* out, int R,
+                              int n_split, int D, cudaStream_t stream);
+
+/* Free every library-owned workspace (synchronises the devices that own one). */
+ATTN_API int attn_release_workspace(void);
+
+/*
+ * Read the device error word of the current device (synchronises the device).
+ * *code receives the raw bits (1 timeout, 2 negative block id, 4 seq_len
+ * beyond the table); the return is ATTN_OK if it is 0, else ATTN_ERR_TIMEOUT
+ * or ATTN_ERR_BAD_INPUT.  reset != 0 clears it.
+ */
+ATTN_API int attn_get_device_error(int* code, int reset);
+
+/* cudaError_t value behind the last ATTN_ERR_CUDA returned on this thread. */
+ATTN_API int attn_last_cuda_error(void);
+
+/* Static description of a status code. */
+ATTN_API const char* attn_status_string(int status);
+
+/* Library version: major*10000 + minor*100 + patch. */
+ATTN_API int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

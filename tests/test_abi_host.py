@@ -1,0 +1,124 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds and loads,
+exports every entry point include/attn.h declares, and rejects bad arguments
+before launching anything.  Pointers here are fake addresses: every call below
+returns from argument validation without touching the device."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import attention_gqa_causal_gb300 as ag
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+P = ctypes.c_void_p
+A16 = 0x10000          # a 16-byte aligned fake device address
+A16B = 0x20000000
+MIS = 0x10008          # 8-byte aligned only
+
+
+def declared():
+    text = open(HEADER).read()
+    return re.findall(r"ATTN_API\s+[\w\s\*]+?\b(attn_\w+)\s*\(", text)
+
+
+def test_header_declares_all_bound_symbols():
+    names = set(declared())
+    assert names == set(ag.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ag.load()
+    for name in declared():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (attn_\w+)", out))
+    assert set(declared()) <= exported
+
+
+def test_version_and_status_strings():
+    assert ag.attn_version() == 100
+    assert ag.status_string(0) == "ok"
+    for code in (-1, -2, -3, -4, -5, -6):
+        assert ag.status_string(code) not in ("ok", "unknown status")
+    assert ag.status_string(-99) == "unknown status"
+
+
+def prefill(Q=A16, K=A16 + 0x100000, V=A16 + 0x200000, O=A16B, B=1, S=64, Hq=4, Hkv=2, D=128, causal=1):
+    return ag.load().attn_prefill(P(Q), P(K), P(V), P(O), B, S, Hq, Hkv, D, causal, P(0))
+
+
+def test_prefill_validation():
+    assert prefill(D=64) == ag.ATTN_ERR_UNSUPPORTED
+    assert prefill(D=256) == ag.ATTN_ERR_UNSUPPORTED
+    assert prefill(Hq=6, Hkv=4) == ag.ATTN_ERR_INVALID_ARG
+    assert prefill(Hq=0) == ag.ATTN_ERR_INVALID_ARG
+    assert prefill(Hkv=0) == ag.ATTN_ERR_INVALID_ARG
+    assert prefill(B=-1) == ag.ATTN_ERR_INVALID_ARG
+    assert prefill(S=-5) == ag.ATTN_ERR_INVALID_ARG
+    assert prefill(Q=0) == ag.ATTN_ERR_INVALID_ARG
+    assert prefill(O=0) == ag.ATTN_ERR_INVALID_ARG
+    assert prefill(K=MIS) == ag.ATTN_ERR_INVALID_ARG
+    assert prefill(O=A16 + 64) == ag.ATTN_ERR_INVALID_ARG      # O overlaps Q
+    assert prefill(O=A16 + 0x100000 + 16) == ag.ATTN_ERR_INVALID_ARG  # O overlaps K
+    # empty problems are valid no-ops (nothing launched, no device needed)
+    assert prefill(B=0) == ag.ATTN_OK
+    assert prefill(S=0) == ag.ATTN_OK
+    assert prefill(B=0, Q=0, K=0, V=0, O=0) == ag.ATTN_OK
+
+
+def decode(q=A16, kc=A16 + 0x100000, vc=A16 + 0x200000, out=A16B, bt=A16 + 0x300000, sl=A16 + 0x400000,
+           N=4, Hq=16, Hkv=8, D=128, mb=128, bs=16):
+    return ag.load().attn_decode_paged(P(q), P(kc), P(vc), P(out), P(bt), P(sl), N, Hq, Hkv, D, mb, bs, P(0))
+
+
+def test_decode_validation():
+    assert decode(bs=32) == ag.ATTN_ERR_UNSUPPORTED
+    assert decode(bs=8) == ag.ATTN_ERR_UNSUPPORTED
+    assert decode(D=64) == ag.ATTN_ERR_UNSUPPORTED
+    assert decode(Hq=12, Hkv=8) == ag.ATTN_ERR_INVALID_ARG
+    assert decode(N=-1) == ag.ATTN_ERR_INVALID_ARG
+    assert decode(mb=0) == ag.ATTN_ERR_INVALID_ARG
+    assert decode(bt=0) == ag.ATTN_ERR_INVALID_ARG
+    assert decode(sl=A16 + 2) == ag.ATTN_ERR_INVALID_ARG
+    assert decode(kc=MIS) == ag.ATTN_ERR_INVALID_ARG
+    assert decode(out=A16 + 32) == ag.ATTN_ERR_INVALID_ARG      # out overlaps q
+    assert decode(N=0) == ag.ATTN_OK
+    assert decode(N=0, q=0, kc=0, vc=0, out=0, bt=0, sl=0) == ag.ATTN_OK
+
+
+def test_workspace_sizes_and_checks():
+    ws = ag.attn_decode_paged_workspace_bytes
+    # default split of 16 pages: 128 pages -> 8 splits; [N*H_q*8*128] f32 + [N*H_q*8] f32, 256-aligned
+    n = ws(256, 16, 8, 128, 128, 16, 0)
+    assert n == 256 * 16 * 8 * 128 * 4 + ((256 * 16 * 8 * 4 + 255) // 256) * 256
+    assert ws(256, 16, 8, 128, 128, 16, 1) == 256 * 16 * 128 * 128 * 4 + 256 * 16 * 128 * 4
+    assert ws(8, 16, 8, 128, 2048, 16, 16) == 8 * 16 * 128 * 128 * 4 + ((8 * 16 * 128 * 4 + 255) // 256) * 256
+    assert ws(4, 16, 8, 64, 128, 16, 0) == 0
+    assert ws(4, 16, 8, 128, 128, 32, 0) == 0
+    lib = ag.load()
+    need = ws(4, 16, 8, 128, 128, 16, 0)
+    args = [P(A16), P(A16 + 0x100000), P(A16 + 0x200000), P(A16B), P(A16 + 0x300000), P(A16 + 0x400000),
+            4, 16, 8, 128, 128, 16, 0]
+    assert lib.attn_decode_paged_ws(*args, P(0x40000000), need - 1, P(0)) == ag.ATTN_ERR_WORKSPACE
+    assert lib.attn_decode_paged_ws(*args, P(0), need, P(0)) == ag.ATTN_ERR_WORKSPACE
+    assert lib.attn_decode_paged_ws(*args, P(0x40000010), need, P(0)) == ag.ATTN_ERR_WORKSPACE
+
+
+def test_combine_validation():
+    lib = ag.load()
+    assert lib.attn_lse_combine(P(A16), P(A16B), P(A16 + 0x300000), 4, 3, 64, P(0)) == ag.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_lse_combine(P(A16), P(A16B), P(A16 + 0x300000), -1, 3, 128, P(0)) == ag.ATTN_ERR_INVALID_ARG
+    assert lib.attn_lse_combine(P(A16), P(A16B), P(A16 + 0x300000), 4, 0, 128, P(0)) == ag.ATTN_ERR_INVALID_ARG
+    assert lib.attn_lse_combine(P(0), P(A16B), P(A16 + 0x300000), 4, 3, 128, P(0)) == ag.ATTN_ERR_INVALID_ARG
+    assert lib.attn_lse_combine(P(0), P(0), P(0), 0, 3, 128, P(0)) == ag.ATTN_OK
+
+
+def test_binding_rejects_cpu_tensors():
+    import torch
+    x = torch.zeros(1, 4, 2, 128, dtype=torch.float16)
+    with pytest.raises(ValueError):
+        ag.attn_prefill(x, x[:, :, :1], x[:, :, :1], x.clone())

@@ -1,0 +1,129 @@
+"""GPU parity of attn_prefill (called through the C ABI) against the FP64 oracle.
+
+Covers the pages' own test shapes, the small and Qwen3-shaped workloads in
+full, the long workload (B=2, S=8192, H 32/8, causal and full) on sampled rows
+with the launch configuration the benchmark times, ragged sequence lengths
+around the 128-row tiles, group sizes 1..8 (even groups pair heads in a CTA,
+odd ones pair row tiles), and the closed-form invariants."""
+import numpy as np
+import pytest
+import torch
+
+import attention_gqa_causal_gb300 as ag
+import golden_cases
+import oracle
+import workloads as W
+from gpu_util import assert_close, dev, device_error_clean, host
+
+pytestmark = pytest.mark.gpu
+
+
+def run_prefill(Q, K, V, causal=True):
+    O = torch.empty(Q.shape, dtype=torch.float16, device="cuda")
+    ag.attn_prefill(dev(Q), dev(K), dev(V), O, causal=causal)
+    torch.cuda.synchronize()
+    return host(O)
+
+
+def rand_inputs(B, S, H_q, H_kv, seed):
+    cfg = W.PrefillConfig("t", B, S, H_q, H_kv)
+    return W.prefill_inputs(cfg, seed=seed)
+
+
+@pytest.mark.parametrize("case", golden_cases.load()[0])
+def test_page_prefill_cases(case):
+    B, S, H_q, H_kv, D = case
+    Q, K, V = rand_inputs(B, S, H_q, H_kv, seed=S)
+    assert_close(run_prefill(Q, K, V), oracle.prefill(Q, K, V), f"page case {case}")
+    assert device_error_clean()
+
+
+def test_small_workload_seed0():
+    cfg = W.PREFILL_SMALL
+    Q, K, V = W.prefill_inputs(cfg, seed=0)
+    assert_close(run_prefill(Q, K, V), oracle.prefill(Q, K, V), cfg.name)
+
+
+@pytest.mark.parametrize("S", [1, 2, 17, 127, 128, 129, 255, 256, 300, 383, 513])
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("heads", [(4, 2), (3, 3), (6, 2), (8, 1)])
+def test_ragged_lengths_and_groups(S, causal, heads):
+    H_q, H_kv = heads
+    Q, K, V = rand_inputs(2, S, H_q, H_kv, seed=S * 7 + H_q)
+    assert_close(run_prefill(Q, K, V, causal), oracle.prefill(Q, K, V, causal=causal),
+                 f"S={S} causal={causal} heads={heads}")
+
+
+def test_qwen_shape_full_compare():
+    cfg = W.PREFILL_QWEN
+    Q, K, V = W.prefill_inputs(cfg, seed=0)
+    assert_close(run_prefill(Q, K, V), oracle.prefill(Q, K, V), cfg.name)
+    assert device_error_clean()
+
+
+def _sample_rows(cfg, n, seed):
+    rng = np.random.default_rng(seed)
+    rows = [(b, i, h) for b in range(cfg.B) for i in (0, 1, 127, 128, cfg.S - 129, cfg.S - 1)
+            for h in (0, cfg.H_q - 1)]
+    rows += [(int(rng.integers(cfg.B)), int(rng.integers(cfg.S)), int(rng.integers(cfg.H_q)))
+             for _ in range(n)]
+    return np.array(rows, np.int32)
+
+
+@pytest.mark.parametrize("cfg", [W.PREFILL_LONG, W.PREFILL_LONG_FULL], ids=lambda c: c.name)
+def test_long_workload_sampled_rows(cfg):
+    Q, K, V = W.prefill_inputs(cfg, seed=0)
+    O = run_prefill(Q, K, V, cfg.causal)
+    rows = _sample_rows(cfg, 160, seed=1)
+    ref = oracle.prefill_rows(Q, K, V, rows, causal=cfg.causal)
+    got = O[rows[:, 0], rows[:, 1], rows[:, 2]]
+    assert_close(got, ref, cfg.name)
+    assert np.isfinite(O.astype(np.float32)).all()
+    assert device_error_clean()
+
+
+def test_invariants_identical_v_row0_and_determinism():
+    B, S, H_q, H_kv = 2, 300, 8, 2
+    Q, K, V = rand_inputs(B, S, H_q, H_kv, seed=5)
+    # identical V rows: the output is that row (to FP16 rounding of a weighted mean of equal values)
+    Vc = np.broadcast_to(V[:, :1], V.shape).copy()
+    O = run_prefill(Q, K, Vc)
+    g = (np.arange(H_q) * H_kv) // H_q
+    expect = np.broadcast_to(Vc[:, :1][:, :, g, :], O.shape).astype(np.float64)
+    assert_close(O, expect, "identical V rows")
+    # causal row 0 attends to V[0] alone (weight 1 up to the rounding of exp2 near 0)
+    O = run_prefill(Q, K, V)
+    assert_close(O[:, 0], V[:, 0][:, g].astype(np.float64), "causal row 0", max_abs=1e-3, mean_abs=1e-5)
+    # identical K rows: causal row i is the mean of V[0..i]
+    Kc = np.broadcast_to(K[:, :1], K.shape).copy()
+    O = run_prefill(Q, Kc, V)
+    Vd = V.astype(np.float64)
+    means = np.cumsum(Vd, axis=1) / np.arange(1, S + 1)[None, :, None, None]
+    assert_close(O, means[:, :, g, :], "identical K rows")
+    # run-to-run determinism
+    a = run_prefill(Q, K, V)
+    b = run_prefill(Q, K, V)
+    assert np.array_equal(a, b)
+
+
+def test_mha_equals_per_head():
+    B, S, H = 1, 200, 3
+    Q, K, V = rand_inputs(B, S, H, H, seed=9)
+    O = run_prefill(Q, K, V)
+    for h in range(H):
+        Oh = run_prefill(Q[:, :, h:h + 1].copy(), K[:, :, h:h + 1].copy(), V[:, :, h:h + 1].copy())
+        assert np.array_equal(O[:, :, h:h + 1], Oh)
+
+
+def test_empty_problem_is_noop():
+    Q = torch.zeros(1, 0, 4, 128, dtype=torch.float16, device="cuda")
+    K = torch.zeros(1, 0, 2, 128, dtype=torch.float16, device="cuda")
+    ag.attn_prefill(Q, K, K, Q.clone())
+    torch.cuda.synchronize()
+
+
+def test_unsupported_head_dim_raises():
+    Q = torch.zeros(1, 8, 2, 64, dtype=torch.float16, device="cuda")
+    with pytest.raises(ag.AttnError) as e:
+        ag.attn_prefill(Q, Q[:, :, :1].contiguous(), Q[:, :, :1].contiguous(), Q.clone())
+    assert e.value.status == ag.ATTN_ERR_UNSUPPORTED
