@@ -1,0 +1,410 @@
+#!/usr/bin/env python
+"""Benchmark of the attention hot path on one GB300 (or N, one process each).
+
+One step is one pass over every hot-path kernel on its workload:
+  * causal GQA prefill   B=2, S=8192, H_q=32, H_kv=8, D=128   (headline: TFLOP/s,
+    causal FLOPs counted as 2*B*H_q*S^2*D)
+  * the same shape without the mask (the unmasked tensor-core ceiling)
+  * paged decode          256 sequences, lengths uniform on [128, 2048], H 16/8
+  * paged decode          8 sequences x 32768 tokens, H 16/8
+    (decode: GB/s of K/V bytes of the valid tokens; split-K + combine kernels)
+Each kernel launch is bracketed by CUDA events on the stream it runs on; the
+K timed steps are bracketed by a barrier and a device synchronisation.  All
+inputs are resident in HBM and larger than L2 (129 MB), so no flush is done.
+
+--impl reference times the FP64 CPU oracle instead (bounded row samples of the
+same prefill workload on the host cores): a deliberately slow baseline.
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs the same work on
+its own GPU (weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "prefill attn TFLOP/s; paged-decode KV-read GB/s (fraction of GB300 peak)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = {
+    "prefill_kernel": ["prefill.cu", "ptx.cuh"],
+    "decode_splitk_kernel": ["decode.cu"],
+}
+
+
+# ------------------------------------------------------------------ helpers
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def dist_init(world: int, use_cuda: bool):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group("nccl" if use_cuda else "gloo")
+    return dist
+
+
+def reduce_max(dist, x: float, use_cuda: bool) -> float:
+    """Max of a float over ranks (identity without a process group)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if use_cuda else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash(kernel: str) -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "attention_gqa_causal_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def dram_traffic(kernel: str, workload: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)
+        e = t[kernel][workload]
+        return e["bytes_per_launch"] if e.get("source_hash") == source_hash(kernel) else None
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        self.p.wait()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[0]))
+                mx = float(r[1])
+                for name, v in zip(names, r[4:8]):
+                    if v.strip().lower() == "active":
+                        reasons.add(name)
+            except (ValueError, IndexError):
+                continue
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ GPU legs
+
+class Leg:
+    def __init__(self, name, kind, work, unit, launches):
+        self.name, self.kind, self.work, self.unit, self.launches = name, kind, work, unit, launches
+        self.times = []
+
+    def value(self, ms):
+        return self.work / (ms * 1e-3) / (1e12 if self.unit == "TFLOP/s" else 1e9)
+
+
+def build_legs(torch, ag, which):
+    legs = []
+    if which in ("all", "prefill", "prefill_full"):
+        Q, K, V = W.prefill_inputs(W.PREFILL_LONG, seed=0)
+        dQ, dK, dV = (torch.from_numpy(x).cuda() for x in (Q, K, V))
+        dO = torch.empty_like(dQ)
+        host = {"Q": Q, "K": K, "V": V}
+        for cfg in ((W.PREFILL_LONG,) if which == "prefill" else (W.PREFILL_LONG_FULL,)
+                    if which == "prefill_full" else (W.PREFILL_LONG, W.PREFILL_LONG_FULL)):
+            leg = Leg(cfg.name, "prefill", cfg.flops(), "TFLOP/s", 1)
+            leg.cfg = cfg
+            leg.run = (lambda c=cfg: ag.attn_prefill(dQ, dK, dV, dO, causal=c.causal))
+            leg.host, leg.dev_in, leg.dev_out = host, (dQ, dK, dV), dO
+            leg.config = {"B": cfg.B, "S": cfg.S, "H_q": cfg.H_q, "H_kv": cfg.H_kv, "D": cfg.D,
+                          "causal": cfg.causal}
+            legs.append(leg)
+    for cfg, key in ((W.DECODE_MIX, "decode"), (W.DECODE_LONG, "decode_long")):
+        if which not in ("all", key):
+            continue
+        inp = W.decode_inputs(cfg, seed=0)
+        t = [torch.from_numpy(x).cuda() for x in (inp.q, inp.k_cache, inp.v_cache,
+                                                  inp.block_tables, inp.seq_lens)]
+        out = torch.empty_like(t[0])
+        leg = Leg(cfg.name, "decode", float(inp.kv_bytes()), "GB/s", 2)
+        leg.run = (lambda t=t, out=out: ag.attn_decode_paged(t[0], t[1], t[2], out, t[3], t[4]))
+        leg.host = {"q": inp.q, "k_cache": inp.k_cache, "v_cache": inp.v_cache,
+                    "block_tables": inp.block_tables, "seq_lens": inp.seq_lens}
+        leg.dev_in, leg.dev_out = tuple(t), out
+        leg.config = {"num_seqs": cfg.num_seqs, "H_q": cfg.H_q, "H_kv": cfg.H_kv, "D": cfg.D,
+                      "block_size": cfg.block_size, "seq_len": [cfg.len_lo, cfg.len_hi],
+                      "max_blocks_per_seq": cfg.max_blocks_per_seq,
+                      "num_blocks": inp.num_blocks, "kv_bytes": inp.kv_bytes()}
+        legs.append(leg)
+    return legs
+
+
+def time_device(torch, legs, steps, warmup, dist, use_cuda):
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        for leg in legs:
+            leg.run()
+    torch.cuda.synchronize()
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in legs] for _ in range(steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for s in range(steps):
+        for i, leg in enumerate(legs):
+            ev[s][i][0].record(stream)
+            leg.run()
+            ev[s][i][1].record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    wall = time.perf_counter() - t0
+    for i, leg in enumerate(legs):
+        leg.times = [ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(steps)]
+    return wall
+
+
+def time_e2e(torch, leg, steps, warmup):
+    """Same leg through the public API with pinned host buffers: H2D of the
+    inputs, the C-ABI call, D2H of the output, all inside the timed region."""
+    pinned_in = [torch.from_numpy(np.ascontiguousarray(x)).pin_memory() for x in leg.host.values()]
+    pinned_out = torch.empty(leg.dev_out.shape, dtype=leg.dev_out.dtype).pin_memory()
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for h, d in zip(pinned_in, leg.dev_in):
+            d.copy_(h, non_blocking=True)
+        leg.run()
+        pinned_out.copy_(leg.dev_out, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    bi = sum(x.numel() * x.element_size() for x in pinned_in)
+    bo = pinned_out.numel() * pinned_out.element_size()
+    return {"value": leg.value(ms), "unit": leg.unit, "ms": ms,
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def oracle_sample(seconds: float, seed: int = 0):
+    """Time the FP64 oracle on random rows of the causal prefill workload until
+    about `seconds` of CPU time; returns (TFLOP/s, rows, wall seconds, threads)."""
+    import oracle
+    cfg = W.PREFILL_LONG
+    Q, K, V = W.prefill_inputs(cfg, seed=0)
+    rng = np.random.default_rng(seed)
+    threads = oracle.num_threads()
+
+    def rows(n):
+        return np.stack([rng.integers(cfg.B, size=n), rng.integers(cfg.S, size=n),
+                         rng.integers(cfg.H_q, size=n)], 1).astype(np.int32)
+
+    def flops(r):  # QK^T and PV over the i+1 allowed keys of each row
+        return float(np.sum(4.0 * cfg.D * (r[:, 1].astype(np.float64) + 1)))
+
+    n = 2 * threads
+    r = rows(n)
+    t = time.perf_counter()
+    oracle.prefill_rows(Q, K, V, r, causal=True)
+    dt = time.perf_counter() - t
+    total_f, total_t, total_n = flops(r), dt, n
+    while total_t < seconds:
+        n = int(min(max(n, (seconds - total_t) / max(dt, 1e-3) * n * 0.5), 200000)) or 1
+        r = rows(n)
+        t = time.perf_counter()
+        oracle.prefill_rows(Q, K, V, r, causal=True)
+        dt = time.perf_counter() - t
+        total_f += flops(r)
+        total_t += dt
+        total_n += n
+    return total_f / total_t / 1e12, total_n, total_t, threads
+
+
+# ------------------------------------------------------------------ arms
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = dist_init(world, True)
+    import attention_gqa_causal_gb300 as ag
+    ag.load()
+    legs = build_legs(torch, ag, args.workload)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    wall = time_device(torch, legs, args.steps, args.warmup, dist, True)
+    clk = clocks.stop()
+    wall = reduce_max(dist, wall, True)
+    err = ag.attn_get_device_error(reset=True)
+    peaks, peak_src = load_peaks()
+
+    parts = []
+    for leg in legs:
+        ms = reduce_max(dist, sum(leg.times) / len(leg.times), True)
+        val = leg.value(ms) * world
+        part = {"workload": leg.name, "value": val, "unit": leg.unit, "ms": ms,
+                "ms_min": min(leg.times), "config": leg.config}
+        if leg.kind == "prefill":
+            peak = peaks["bf16_tflops"]
+            part["roofline"] = {"bound": "tensor", "achieved": leg.value(ms), "peak": peak,
+                                "unit": "TFLOP/s", "frac": leg.value(ms) / peak,
+                                "peak_kind": f"{peak_src} dense bf16 burst (fp16 runs at the same tensor rate)",
+                                "traffic": dram_traffic("prefill_kernel", leg.name)}
+        else:
+            peak = peaks["hbm_gbs"]
+            part["roofline"] = {"bound": "hbm", "achieved": leg.value(ms), "peak": peak,
+                                "unit": "GB/s", "frac": leg.value(ms) / peak,
+                                "peak_kind": f"{peak_src} copy bandwidth",
+                                "traffic": dram_traffic("decode_splitk_kernel", leg.name)}
+        parts.append(part)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e_parts = {}
+        for leg in legs:
+            e2e_parts[leg.name] = time_e2e(torch, leg, max(2, min(args.steps, 10)), 2)
+        head = legs[0].name
+        e2e = dict(e2e_parts[head])
+        e2e["workload"] = head
+        for p in parts:
+            p["e2e"] = e2e_parts[p["workload"]]
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        tf, n, secs, threads = oracle_sample(args.cpu_seconds)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"{n} random rows (b,i,h) of {W.PREFILL_LONG.name}, FP64, {secs:.1f} s"}
+
+    head = parts[0]
+    launches = sum(leg.launches for leg in legs) * args.steps
+    line = {
+        "metric": METRIC, "value": head["value"], "unit": head["unit"], "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": wall * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic: seeded N(0,1) FP16 "
+        "(splitmix64 + Box-Muller), seq_lens uniform, block tables a seeded permutation",
+        "config": {"workload": " + ".join(leg.name for leg in legs), **head["config"],
+                   "l2": "inputs larger than L2 (129 MB); no flush",
+                   "parallelism": f"replicated weak scaling x{world}" if world > 1 else "single GPU"},
+        "roofline": head["roofline"], "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": launches, "clocks": clk, "device_error": err, "parts": parts,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    secs = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup) * 3)
+    vals = []
+    n_tot = 0
+    t_tot = 0.0
+    threads = 1
+    for s in range(args.warmup + args.steps):
+        tf, n, t, threads = oracle_sample(secs, seed=s)
+        if s >= args.warmup:
+            vals.append(tf)
+            n_tot += n
+            t_tot += t
+    val = statistics.mean(vals)
+    sample = f"{n_tot} random rows (b,i,h) of {W.PREFILL_LONG.name} over {args.steps} steps, FP64, {t_tot:.1f} s"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_tot * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic: seeded N(0,1) FP16 inputs, FP64 CPU oracle",
+        "config": {"workload": W.PREFILL_LONG.name, "B": 2, "S": 8192, "H_q": 32, "H_kv": 8,
+                   "D": 128, "causal": True},
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["all", "prefill", "prefill_full", "decode", "decode_long"],
+                    default="all")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="CPU time budget of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
