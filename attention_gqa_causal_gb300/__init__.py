@@ -18,8 +18,10 @@ from ._binding import (  # noqa: F401
     ATTN_ERR_WORKSPACE,
     ATTN_OK,
     EXPORTED,
+    NOALLOC_SCRATCH_BYTES,
     AttnError,
     attn_decode_paged,
+    attn_decode_paged_noalloc,
     attn_decode_paged_workspace_bytes,
     attn_decode_paged_ws,
     attn_get_device_error,

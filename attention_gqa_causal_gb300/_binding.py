@@ -26,7 +26,11 @@ EXPORTED = [
     "attn_prefill", "attn_decode_paged", "attn_decode_paged_workspace_bytes",
     "attn_decode_paged_ws", "attn_lse_combine", "attn_release_workspace",
     "attn_get_device_error", "attn_last_cuda_error", "attn_status_string", "attn_version",
+    "attn_decode_paged_noalloc",
 ]
+
+# Size of the scratch buffer compiled into the library for attn_decode_paged_noalloc.
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 _lock = threading.Lock()
 _lib = None
@@ -61,6 +65,7 @@ def load():
             lib.attn_status_string.argtypes = [i]
             lib.attn_status_string.restype = ctypes.c_char_p
             lib.attn_version.argtypes = []
+            lib.attn_decode_paged_noalloc.argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, p]
             _lib = lib
     return _lib
 
@@ -148,6 +153,25 @@ def attn_decode_paged_ws(q, k_cache, v_cache, out, block_tables, seq_lens,
     _check(load().attn_decode_paged_ws(*ptrs, *sizes, int(pages_per_split),
                                        ctypes.c_void_p(workspace.data_ptr()), nbytes,
                                        ctypes.c_void_p(st)), "attn_decode_paged_ws")
+
+
+def attn_decode_paged_noalloc(q, k_cache, v_cache, out, block_tables, seq_lens,
+                              stream=None) -> None:
+    """attn_decode_paged for callers that cannot allocate device memory.
+
+    Meant for code that has no CUDA allocator of its own to call (for example
+    when another runtime owns all device memory), that runs under a fixed
+    memory budget, or that must not risk the device-wide synchronisation of
+    cudaMalloc/cudaFree.  The split-K scratch is a fixed NOALLOC_SCRATCH_BYTES
+    buffer inside the library, so nothing is allocated; a problem that needs
+    more scratch raises AttnError(ATTN_ERR_WORKSPACE).  The first call on a
+    device looks the buffer up (make it before any stream capture), and calls
+    that overlap on the GPU share the buffer and race: serialise them.
+    """
+    ptrs, sizes = _decode_args(q, k_cache, v_cache, out, block_tables, seq_lens)
+    st = _stream(stream, q.device)
+    _check(load().attn_decode_paged_noalloc(*ptrs, *sizes, ctypes.c_void_p(st)),
+           "attn_decode_paged_noalloc")
 
 
 def attn_lse_combine(O_part: torch.Tensor, lse: torch.Tensor, out: torch.Tensor,

@@ -95,6 +95,8 @@ int validate_decode(const void* q, const void* k_cache, const void* v_cache, voi
 
 }  // namespace
 
+int attn::record_cuda_error(cudaError_t e) { return cuda_fail(e); }
+
 extern "C" {
 
 ATTN_API int attn_prefill(const void* Q, const void* K, const void* V, void* O, int B, int S,

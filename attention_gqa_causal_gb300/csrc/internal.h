@@ -47,6 +47,10 @@ cudaError_t launch_decode(const DecodePlan& p, const void* q, const void* k_cach
 cudaError_t launch_lse_combine(const float* O_part, const float* lse_part, void* out, int R,
                                int n_split, cudaStream_t stream);
 
+// Store `e` as this thread's last CUDA error (attn_last_cuda_error) and
+// return ATTN_ERR_CUDA; defined in api.cu.
+int record_cuda_error(cudaError_t e);
+
 // Prefill: O = softmax(Q K^T / sqrt(D), causal) V over [B,S,H,D] tensors.
 cudaError_t launch_prefill(const void* Q, const void* K, const void* V, void* O, int B, int S,
                            int H_q, int H_kv, int causal, cudaStream_t stream);

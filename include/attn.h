@@ -109,6 +109,34 @@ ATTN_API int attn_decode_paged_ws(const void* q, const void* k_cache, const void
                                   size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * attn_decode_paged for callers that cannot allocate device memory.
+ * The pages have no counterpart of this call.  It is for users of this
+ * library who cannot call cudaMalloc: code hosted in another runtime that
+ * owns all device memory and offers no allocator, programs under a fixed
+ * memory budget, and loops that must not risk the device-wide
+ * synchronisation cudaMalloc/cudaFree can bring.
+ * Same arguments, semantics and preconditions as attn_decode_paged.  The
+ * split-K scratch is a buffer of ATTN_NOALLOC_SCRATCH_BYTES (32 MiB)
+ * compiled into the library: every GPU that loads the library's device code
+ * holds it until the process exits.  The call allocates nothing.
+ *  - A problem whose scratch (attn_decode_paged_workspace_bytes with
+ *    pages_per_split = 0) exceeds ATTN_NOALLOC_SCRATCH_BYTES is refused with
+ *    ATTN_ERR_WORKSPACE before anything is launched.
+ *  - The first call on a device looks up the buffer's device address with
+ *    cudaGetSymbolAddress; make that first call before any stream capture.
+ *  - Every call on a device shares the one buffer, which keeps the last
+ *    call's contents.  Nothing needs clearing (each partial that is read is
+ *    written earlier in the same call), but calls that overlap on the GPU
+ *    (e.g. on two streams) race on it: serialise them.
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+ATTN_API int attn_decode_paged_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                       void* out, const int* block_tables, const int* seq_lens,
+                                       int num_seqs, int H_q, int H_kv, int D,
+                                       int max_blocks_per_seq, int block_size,
+                                       cudaStream_t stream);
+
+/*
  * Merge partial attention results over disjoint key segments by their
  * log-sum-exp (the combine step of split-K decode):
  *   L = log sum_i exp(lse[r,i]),  out[r,:] = sum_i exp(lse[r,i] - L) O_part[r,i,:]
