@@ -16,6 +16,7 @@ enum DeviceError : int {
     kDevErrBadBlockId = 2,     // a block_tables entry < 0 inside a sequence's range
     kDevErrSeqTooLong = 4,     // seq_lens[n] > max_blocks_per_seq * block_size
     kDevErrTmemAlloc = 8,      // TMEM base address outside the expected range
+    kDevErrSmemLayout = 16,    // dynamic shared memory base too misaligned for the tile layout
 };
 
 // Set by the kernels (atomicOr); defined in decode.cu.  Device address of the

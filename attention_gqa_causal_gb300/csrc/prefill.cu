@@ -12,26 +12,32 @@
 // tile on tensor-core scores.
 //
 // GB300 design (one CTA per SM, 320 threads):
-//   warps 0-3  softmax warpgroup 0  (Q tile 0, TMEM lanes 0..127 = its rows)
-//   warps 4-7  softmax warpgroup 1  (Q tile 1)
+//   warps 0-3  softmax of Q tile 0 (TMEM lanes 0..127 = its rows)
+//   warps 4-7  softmax of Q tile 1
 //   warp  8    MMA issuer (one lane) + TMEM allocation
 //   warp  9    TMA producer (one lane)
 // A CTA owns two 128-row Q tiles that read the same K/V: two query heads of
 // one GQA group over the same rows when the group size is even (identical
 // causal extents), else two consecutive row tiles of one head.  Per 128-key
-// tile j the MMA warp computes S_t = Q_t K_j^T into TMEM (FP32), softmax
-// warpgroup t turns its row of S_t into P_t = exp2(S*c - m) and writes P_t
-// back over S_t in TMEM as FP16, and the MMA warp accumulates
-// O_t += P_t V_j with A read from TMEM.  The two tiles ping-pong: while one
-// warpgroup runs its softmax the tensor core works on the other tile.
+// tile j the MMA warp computes S_t = Q_t K_j^T into TMEM (FP32), the softmax
+// warps of tile t turn S_t into P_t = exp2(S*c - m) and write P_t back over
+// S_t in TMEM as FP16, and the MMA warp accumulates O_t += P_t V_j with A read
+// from TMEM.  The two tiles ping-pong: while one tile runs its softmax the
+// tensor core works on the other.
+// The row maximum is kept lazily: m is a reference that only moves when the
+// row max exceeds it by more than kRescaleThreshold (log2 units); O and l
+// always refer to the same m, so the result is exact.  Because m rarely moves
+// after the first key tile, the exponentials of a tile are computed
+// optimistically against the current m while the tile's max is reduced
+// alongside; in the rare case that the max exceeds the threshold, the warp
+// reloads S (still intact in TMEM: P has not been written yet), moves m,
+// rescales O and recomputes.  This keeps the max reduction off the path from
+// "S ready" to "P ready" that the tensor core waits for.
 // TMEM: S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512) columns.
-// SMEM: Q0,Q1 (32 KB each), 2 K stages, 2 V stages (32 KB each), all
-// 128-byte swizzled as written by TMA boxes of 64 x 128.
-// The running max is rescaled lazily: O and l are rescaled only when the row
-// max grows by more than kRescaleThreshold (log2 units), which keeps the
-// result exact (m, l and O always refer to the same reference max) while
-// making the TMEM read-modify-write of O rare.  Key tiles wholly above the
-// diagonal are never loaded or multiplied; only the diagonal tile is masked.
+// SMEM: Q0,Q1 (32 KB each), 2 K stages, 3 V stages (32 KB each), all
+// 128-byte swizzled as written by TMA boxes of 64 x 128.  Key tiles wholly
+// above the diagonal are never loaded or multiplied; only the diagonal tile
+// is masked.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -50,15 +56,18 @@ namespace {
 constexpr int BM = 128;  // query rows per tile
 constexpr int BN = 128;  // keys per tile
 constexpr int D = kHeadDim;
-constexpr int kThreads = 320;
-constexpr int kStages = 2;
+constexpr int kMmaWarp = 8;
+constexpr int kTmaWarp = 9;
+constexpr int kThreads = 10 * 32;
+constexpr int kKStages = 2;
+constexpr int kVStages = 3;
 constexpr uint32_t kTileBytes = BM * D * 2;      // 32 KB
 constexpr uint32_t kBoxBytes = kTileBytes / 2;   // 16 KB: 128 rows x 64 halves
 constexpr uint32_t kSmemQ = 0;
 constexpr uint32_t kSmemK = 2 * kTileBytes;
-constexpr uint32_t kSmemV = kSmemK + kStages * kTileBytes;
-constexpr uint32_t kSmemBytes = kSmemV + kStages * kTileBytes;
-constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;  // slack for 1024-byte alignment
+constexpr uint32_t kSmemV = kSmemK + kKStages * kTileBytes;
+constexpr uint32_t kSmemBytes = kSmemV + kVStages * kTileBytes;
+constexpr uint32_t kSmemMax = 232448;               // 227 KB: the per-CTA opt-in limit
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -105,13 +114,20 @@ __device__ __forceinline__ Unit decode_unit(const PrefillArgs& a, int u)
 
 struct SmemCtl {
     uint64_t q_full;
-    uint64_t k_full[kStages], k_empty[kStages];
-    uint64_t v_full[kStages], v_empty[kStages];
+    uint64_t k_full[kKStages], k_empty[kKStages];
+    uint64_t v_full[kVStages], v_empty[kVStages];
     uint64_t s_full[2], p_full[2], o_full[2];
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort;
 };
+
+// Dynamic shared memory: the 1024-aligned tiles, then the control block.  The
+// whole 227 KB is requested; the alignment padding the layout can absorb is
+// what is left over (the kernel checks it at run time).
+constexpr uint32_t kSmemAlloc = kSmemMax;
+constexpr uint32_t kAlignSlack = kSmemMax - kSmemBytes - (uint32_t)sizeof(SmemCtl);
+static_assert(kSmemBytes + sizeof(SmemCtl) <= kSmemMax, "shared memory layout too large");
 
 __device__ __forceinline__ void flag_abort(SmemCtl* c, int* err)
 {
@@ -119,13 +135,50 @@ __device__ __forceinline__ void flag_abort(SmemCtl* c, int* err)
     atomicOr(err, kDevErrTimeout);
 }
 
+// Max over 32 values: independent chains of 3-input max, then a small tree.
+__device__ __forceinline__ float max32(const uint32_t (&r)[32])
+{
+    float m[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int b = k * 8;
+        m[k] = fmax3(fmax3(__uint_as_float(r[b]), __uint_as_float(r[b + 1]), __uint_as_float(r[b + 2])),
+                     fmax3(__uint_as_float(r[b + 3]), __uint_as_float(r[b + 4]), __uint_as_float(r[b + 5])),
+                     fmaxf(__uint_as_float(r[b + 6]), __uint_as_float(r[b + 7])));
+    }
+    return fmaxf(fmax3(m[0], m[1], m[2]), m[3]);
+}
+
+// P = exp2(S*c - m) for 32 columns, packed in place (column pair -> even slot);
+// adds the FP32 values into the 4 packed partial sums rs.
+__device__ __forceinline__ void exp_pack32(uint32_t (&r)[32], float c, float neg_m, float (&rs)[8])
+{
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+        float x0, x1;
+        ffma2(x0, x1, __uint_as_float(r[i]), __uint_as_float(r[i + 1]), c, c, neg_m, neg_m);
+        const float p0 = ex2_approx(x0);
+        const float p1 = ex2_approx(x1);
+        const int k = (i / 2) % 4;
+        fadd2(rs[2 * k], rs[2 * k + 1], p0, p1);
+        r[i] = pack_half2(p0, p1);
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const PrefillArgs a)
 {
-    extern __shared__ uint8_t smem_raw[];
-    __shared__ SmemCtl ctl;
-    const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    if (sbase - raw > kAlignSlack) {
+        // the aligned layout would not fit: do nothing rather than overrun
+        if (threadIdx.x == 0)
+            atomicOr(a.err, kDevErrSmemLayout);
+        return;
+    }
+    SmemCtl& ctl = *reinterpret_cast<SmemCtl*>(smem_raw + (sbase - raw) + kSmemBytes);
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
     const Unit w = decode_unit(a, blockIdx.x);
@@ -134,9 +187,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     if (threadIdx.x == 0) {
         ctl.abort = 0;
         mbar_init(smem_u32(&ctl.q_full), 1);
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kKStages; ++s) {
             mbar_init(smem_u32(&ctl.k_full[s]), 1);
             mbar_init(smem_u32(&ctl.k_empty[s]), 1);
+        }
+        for (int s = 0; s < kVStages; ++s) {
             mbar_init(smem_u32(&ctl.v_full[s]), 1);
             mbar_init(smem_u32(&ctl.v_empty[s]), 1);
         }
@@ -148,7 +203,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         mbar_init(smem_u32(&ctl.mma_done), 1);
         fence_mbar_init();
     }
-    if (warp == 8) {
+    if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(&ctl.tmem_base), 512);
         tmem_relinquish();
     }
@@ -157,7 +212,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     tc_fence_after();
     const uint32_t tmem = ctl.tmem_base;
 
-    if (warp == 9) {
+    if (warp == kTmaWarp) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             tma_prefetch_desc(&tmQ);
@@ -172,25 +227,25 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             int n_k = 0, n_v = 0;  // K / V tiles issued so far
             bool ok = true;
             for (int j = 0; j < w.n_kv && ok; ++j) {
-                const int s = j % kStages;
-                const uint32_t ph = (j / kStages) & 1;
-                ok = mbar_wait(smem_u32(&ctl.k_empty[s]), ph ^ 1, abort);
+                const int sk = j % kKStages;
+                ok = mbar_wait(smem_u32(&ctl.k_empty[sk]), ((j / kKStages) & 1) ^ 1, abort);
                 if (!ok)
                     break;
-                const uint32_t kbar = smem_u32(&ctl.k_full[s]);
+                const uint32_t kbar = smem_u32(&ctl.k_full[sk]);
                 mbar_arrive_expect_tx(kbar, kTileBytes);
                 for (int h = 0; h < 2; ++h)
-                    tma_load_4d(sbase + kSmemK + s * kTileBytes + h * kBoxBytes, &tmK, kbar, h * 64,
-                                w.g, j * BN, w.b);
+                    tma_load_4d(sbase + kSmemK + sk * kTileBytes + h * kBoxBytes, &tmK, kbar,
+                                h * 64, w.g, j * BN, w.b);
                 ++n_k;
-                ok = mbar_wait(smem_u32(&ctl.v_empty[s]), ph ^ 1, abort);
+                const int sv = j % kVStages;
+                ok = mbar_wait(smem_u32(&ctl.v_empty[sv]), ((j / kVStages) & 1) ^ 1, abort);
                 if (!ok)
                     break;
-                const uint32_t vbar = smem_u32(&ctl.v_full[s]);
+                const uint32_t vbar = smem_u32(&ctl.v_full[sv]);
                 mbar_arrive_expect_tx(vbar, kTileBytes);
                 for (int h = 0; h < 2; ++h)
-                    tma_load_4d(sbase + kSmemV + s * kTileBytes + h * kBoxBytes, &tmV, vbar, h * 64,
-                                w.g, j * BN, w.b);
+                    tma_load_4d(sbase + kSmemV + sv * kTileBytes + h * kBoxBytes, &tmV, vbar,
+                                h * 64, w.g, j * BN, w.b);
                 ++n_v;
             }
             if (!ok)
@@ -199,37 +254,44 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             // is released (bounded by time only, not by the abort flag)
             const int no_abort = 0;
             mbar_wait(qbar, 0, &no_abort);
-            for (int s = 0; s < kStages; ++s) {
-                // loads issued into stage s: tiles j < n with j % kStages == s
-                const int ck = n_k > s ? (n_k - s + kStages - 1) / kStages : 0;
-                const int cv = n_v > s ? (n_v - s + kStages - 1) / kStages : 0;
-                if (ck)
-                    mbar_wait(smem_u32(&ctl.k_full[s]), (ck - 1) & 1, &no_abort);
-                if (cv)
-                    mbar_wait(smem_u32(&ctl.v_full[s]), (cv - 1) & 1, &no_abort);
+            for (int s = 0; s < kKStages; ++s) {
+                // loads issued into stage s: tiles j < n_k with j % kKStages == s
+                const int c = n_k > s ? (n_k - s + kKStages - 1) / kKStages : 0;
+                if (c)
+                    mbar_wait(smem_u32(&ctl.k_full[s]), (c - 1) & 1, &no_abort);
+            }
+            for (int s = 0; s < kVStages; ++s) {
+                const int c = n_v > s ? (n_v - s + kVStages - 1) / kVStages : 0;
+                if (c)
+                    mbar_wait(smem_u32(&ctl.v_full[s]), (c - 1) & 1, &no_abort);
             }
         }
-    } else if (warp == 8) {
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc_s = idesc_f16_f32(BM, BN, false, false);
             const uint32_t idesc_o = idesc_f16_f32(BM, D, false, true);
+            // descriptors of the first tile of each region; moving within a region
+            // only adds (byte offset >> 4) to the start-address field (all shared
+            // addresses are below 256 KB, so the 14-bit field cannot overflow)
+            const uint64_t dq = sdesc_sw128(sbase + kSmemQ, 16, 1024);
+            const uint64_t dk = sdesc_sw128(sbase + kSmemK, 16, 1024);
+            const uint64_t dv = sdesc_sw128(sbase + kSmemV, kBoxBytes, 1024);
             auto issue_s = [&](int t, int s) {
-                const uint32_t sK = sbase + kSmemK + s * kTileBytes;
+                const uint64_t aq = dq + ((t * kTileBytes) >> 4);
+                const uint64_t bk = dk + ((s * kTileBytes) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk / 4) * kBoxBytes + (kk % 4) * 32;
-                    mma_f16_ss(tmem + t * BN, sdesc_sw128(sbase + kSmemQ + t * kTileBytes + off, 16, 1024),
-                               sdesc_sw128(sK + off, 16, 1024), idesc_s, kk > 0);
+                    const uint32_t off = ((kk / 4) * kBoxBytes + (kk % 4) * 32) >> 4;
+                    mma_f16_ss(tmem + t * BN, aq + off, bk + off, idesc_s, kk > 0);
                 }
             };
             auto issue_o = [&](int t, int s, bool acc) {
-                const uint32_t sV = sbase + kSmemV + s * kTileBytes;
+                const uint64_t bv = dv + ((s * kTileBytes) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_f16_ts(tmem + 256 + t * D, tmem + t * BN + kk * 8,
-                               sdesc_sw128(sV + kk * 2048, kBoxBytes, 1024), idesc_o,
-                               (acc || kk > 0) ? 1u : 0u);
+                    mma_f16_ts(tmem + 256 + t * D, tmem + t * BN + kk * 8, bv + ((kk * 2048) >> 4),
+                               idesc_o, (acc || kk > 0) ? 1u : 0u);
             };
             bool ok = mbar_wait(smem_u32(&ctl.q_full), 0, abort) &&
                       mbar_wait(smem_u32(&ctl.k_full[0]), 0, abort);
@@ -242,39 +304,39 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 mma_commit(smem_u32(&ctl.k_empty[0]));
             }
             for (int j = 0; j < w.n_kv && ok; ++j) {
-                const int s = j % kStages;
-                const uint32_t ph = (j / kStages) & 1;
-                const int s1 = (j + 1) % kStages;
-                const uint32_t ph1 = ((j + 1) / kStages) & 1;
+                const int sv = j % kVStages;
+                const uint32_t phv = (j / kVStages) & 1;
+                const int sk1 = (j + 1) % kKStages;
+                const uint32_t phk1 = ((j + 1) / kKStages) & 1;
                 const bool more = j + 1 < w.n_kv;
-                ok = mbar_wait(smem_u32(&ctl.v_full[s]), ph, abort) &&
-                     mbar_wait(smem_u32(&ctl.p_full[0]), j & 1, abort);
+                ok = mbar_wait(smem_u32(&ctl.p_full[0]), j & 1, abort) &&
+                     mbar_wait(smem_u32(&ctl.v_full[sv]), phv, abort);
                 if (!ok)
                     break;
                 tc_fence_after();
-                issue_o(0, s, j > 0);
+                issue_o(0, sv, j > 0);
                 if (!more)
                     mma_commit(smem_u32(&ctl.o_full[0]));
                 if (more) {
-                    ok = mbar_wait(smem_u32(&ctl.k_full[s1]), ph1, abort);
+                    ok = mbar_wait(smem_u32(&ctl.k_full[sk1]), phk1, abort);
                     if (!ok)
                         break;
                     tc_fence_after();
-                    issue_s(0, s1);
+                    issue_s(0, sk1);
                     mma_commit(smem_u32(&ctl.s_full[0]));
                 }
                 ok = mbar_wait(smem_u32(&ctl.p_full[1]), j & 1, abort);
                 if (!ok)
                     break;
                 tc_fence_after();
-                issue_o(1, s, j > 0);
-                mma_commit(smem_u32(&ctl.v_empty[s]));
+                issue_o(1, sv, j > 0);
+                mma_commit(smem_u32(&ctl.v_empty[sv]));
                 if (!more)
                     mma_commit(smem_u32(&ctl.o_full[1]));
                 if (more) {
-                    issue_s(1, s1);
+                    issue_s(1, sk1);
                     mma_commit(smem_u32(&ctl.s_full[1]));
-                    mma_commit(smem_u32(&ctl.k_empty[s1]));
+                    mma_commit(smem_u32(&ctl.k_empty[sk1]));
                 }
             }
             if (!ok)
@@ -285,13 +347,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             mbar_wait(smem_u32(&ctl.mma_done), 0, &no_abort);
         }
     } else {
-        // ------------------------------------------------------------ softmax warpgroups
-        const int t = warp / 4;
-        const int row = (warp % 4) * 32 + lane;       // row within the tile = TMEM lane
+        // ------------------------------------------------------------ softmax warps
+        const int t = warp / 4;             // Q tile
+        const int quad = warp % 4;          // TMEM lane quadrant = rows [32*quad, +32)
+        const int row = quad * 32 + lane;   // row within the tile = TMEM lane
         const int my_row0 = t ? w.row0[1] : w.row0[0];
         const int my_head = t ? w.head[1] : w.head[0];
-        const int q_row = my_row0 + row;              // row within the sequence
-        const uint32_t lane_addr = static_cast<uint32_t>((warp % 4) * 32) << 16;
+        const int q_row = my_row0 + row;    // row within the sequence
+        const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t tS = tmem + lane_addr + t * BN;
         const uint32_t tO = tmem + lane_addr + 256 + t * D;
         const float c = a.scale_log2;
@@ -303,56 +366,67 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             if (!ok)
                 break;
             tc_fence_after();
-            uint32_t sr[4][32];
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
-                tmem_ld32(tS + q4 * 32, sr[q4]);
-            tmem_ld_wait();
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
-                reg_fence32(sr[q4]);
-            // mask keys beyond the causal bound / the sequence end
             const int kv0 = j * BN;
             const int limit = a.causal ? min(q_row + 1, a.S) - kv0 : a.S - kv0;
-            if (__any_sync(0xffffffffu, limit < BN)) {
+            const bool masked = __any_sync(0xffffffffu, limit < BN);
+            uint32_t sr[4][32];
+            float rs[8];
+            // Pass over the tile against the current reference max.  On the first
+            // tile (no reference yet) or when this tile's max exceeds the
+            // reference by more than the threshold, it runs a second time after
+            // the reference has moved.
+            bool redo = (j == 0);
+            bool grow = false;
+            float alpha = 1.f;
+            for (int pass = 0; pass < 2; ++pass) {
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4)
+                    tmem_ld32(tS + q4 * 32, sr[q4]);
+                tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (q4 * 32 + i >= limit)
-                            sr[q4][i] = __float_as_uint(-CUDART_INF_F);
-            }
-            float mx = -CUDART_INF_F;
+                for (int q4 = 0; q4 < 4; ++q4)
+                    reg_fence32(sr[q4]);
+                if (masked) {
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
+                    for (int q4 = 0; q4 < 4; ++q4)
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    mx = fmaxf(mx, __uint_as_float(sr[q4][i]));
-            const float m_new = fmaxf(m_ref, mx * c);
-            const bool grow = m_new > m_ref + kRescaleThreshold;
-            float alpha = 1.f;
-            if (grow) {
-                alpha = ex2_approx(m_ref - m_new);
-                m_ref = m_new;
-                l_sum *= alpha;
-            }
-            // P = exp2(S*c - m_ref), packed in place (pair of columns -> even slot)
-            // and written as FP16 over the first 64 columns of S_t
-            const float neg_m = -m_ref;
-            float rs = 0.f;
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-#pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(sr[q4][i]), c, neg_m));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(sr[q4][i + 1]), c, neg_m));
-                    rs += p0 + p1;
-                    sr[q4][i] = pack_half2(p0, p1);
+                        for (int i = 0; i < 32; ++i)
+                            if (q4 * 32 + i >= limit)
+                                sr[q4][i] = __float_as_uint(-CUDART_INF_F);
                 }
+                if (redo) {
+                    // move the reference first (first tile, or the rare fix-up)
+                    const float mx = fmaxf(fmax3(max32(sr[0]), max32(sr[1]), max32(sr[2])), max32(sr[3]));
+                    const float m_new = fmaxf(m_ref, mx * c);
+                    if (m_new > m_ref + kRescaleThreshold) {
+                        grow = true;
+                        alpha = ex2_approx(m_ref - m_new);
+                        m_ref = m_new;
+                        l_sum *= alpha;
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    rs[k] = 0.f;
+                const float neg_m = -m_ref;
+                float mx = -CUDART_INF_F;
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    if (!redo)
+                        mx = fmaxf(mx, max32(sr[q4]));  // reduced alongside the exponentials
+                    exp_pack32(sr[q4], c, neg_m, rs);
+                }
+                if (redo || !__any_sync(0xffffffffu, mx * c > m_ref + kRescaleThreshold))
+                    break;
+                redo = true;  // rare: the optimistic pass used a reference that is too low
             }
+            // S has been read for the last time: P overwrites its first 64 columns
             tmem_st32_even(tS, sr[0], sr[1]);
             tmem_st32_even(tS + 32, sr[2], sr[3]);
-            l_sum += rs;
+            fadd2(rs[0], rs[1], rs[2], rs[3]);
+            fadd2(rs[4], rs[5], rs[6], rs[7]);
+            fadd2(rs[0], rs[1], rs[4], rs[5]);
+            l_sum += rs[0] + rs[1];
             if (j > 0 && __any_sync(0xffffffffu, grow)) {
                 // O_t holds the previous tiles' sum (its last PV completed before
                 // s_full fired and the next PV waits for p_full): bring it to the
@@ -407,7 +481,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 8)
+    if (warp == kMmaWarp)
         tmem_dealloc(tmem, 512);
 }
 
