@@ -20,6 +20,7 @@ from ._binding import (  # noqa: F401
     EXPORTED,
     NOALLOC_SCRATCH_BYTES,
     AttnError,
+    attn_debug_prefill_stall,
     attn_decode_paged,
     attn_decode_paged_noalloc,
     attn_decode_paged_workspace_bytes,

@@ -26,7 +26,7 @@ EXPORTED = [
     "attn_prefill", "attn_decode_paged", "attn_decode_paged_workspace_bytes",
     "attn_decode_paged_ws", "attn_lse_combine", "attn_release_workspace",
     "attn_get_device_error", "attn_last_cuda_error", "attn_status_string", "attn_version",
-    "attn_decode_paged_noalloc",
+    "attn_decode_paged_noalloc", "attn_debug_prefill_stall",
 ]
 
 # Size of the scratch buffer compiled into the library for attn_decode_paged_noalloc.
@@ -66,6 +66,7 @@ def load():
             lib.attn_status_string.restype = ctypes.c_char_p
             lib.attn_version.argtypes = []
             lib.attn_decode_paged_noalloc.argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, p]
+            lib.attn_debug_prefill_stall.argtypes = [p, p, p, p, i, i, i, i, i, i, i, p]
             _lib = lib
     return _lib
 
@@ -112,6 +113,19 @@ def attn_prefill(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.Ten
     st = _stream(stream, Q.device)
     _check(load().attn_prefill(*args, B, S, H_q, K.shape[2], D, int(bool(causal)),
                                ctypes.c_void_p(st)), "attn_prefill")
+
+
+def attn_debug_prefill_stall(Q, K, V, O, stall_tile: int, causal: bool = True, stream=None) -> None:
+    """Failure-detection test hook: attn_prefill with key tile ``stall_tile``
+    withheld, so the kernel's bounded waits run out (about a second) and it
+    reports ATTN_ERR_TIMEOUT through attn_get_device_error."""
+    B, S, H_q, D = Q.shape
+    args = [_dev(Q, "Q", torch.float16), _dev(K, "K", torch.float16),
+            _dev(V, "V", torch.float16), _dev(O, "O", torch.float16)]
+    st = _stream(stream, Q.device)
+    _check(load().attn_debug_prefill_stall(*args, B, S, H_q, K.shape[2], D, int(bool(causal)),
+                                           int(stall_tile), ctypes.c_void_p(st)),
+           "attn_debug_prefill_stall")
 
 
 def _decode_args(q, k_cache, v_cache, out, block_tables, seq_lens):

@@ -97,10 +97,9 @@ int validate_decode(const void* q, const void* k_cache, const void* v_cache, voi
 
 int attn::record_cuda_error(cudaError_t e) { return cuda_fail(e); }
 
-extern "C" {
-
-ATTN_API int attn_prefill(const void* Q, const void* K, const void* V, void* O, int B, int S,
-                          int H_q, int H_kv, int D, int causal, cudaStream_t stream)
+namespace {
+int prefill_checked(const void* Q, const void* K, const void* V, void* O, int B, int S, int H_q,
+                    int H_kv, int D, int causal, int stall_tile, cudaStream_t stream)
 {
     if (B < 0 || S < 0 || check_heads(H_q, H_kv) != ATTN_OK)
         return ATTN_ERR_INVALID_ARG;
@@ -117,8 +116,26 @@ ATTN_API int attn_prefill(const void* Q, const void* K, const void* V, void* O, 
     if (overlap(O, qbytes, Q, qbytes) || overlap(O, qbytes, K, kvbytes) ||
         overlap(O, qbytes, V, kvbytes))
         return ATTN_ERR_INVALID_ARG;
-    const cudaError_t e = attn::launch_prefill(Q, K, V, O, B, S, H_q, H_kv, causal, stream);
+    const cudaError_t e = attn::launch_prefill(Q, K, V, O, B, S, H_q, H_kv, causal, stall_tile, stream);
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+}  // namespace
+
+extern "C" {
+
+ATTN_API int attn_prefill(const void* Q, const void* K, const void* V, void* O, int B, int S,
+                          int H_q, int H_kv, int D, int causal, cudaStream_t stream)
+{
+    return prefill_checked(Q, K, V, O, B, S, H_q, H_kv, D, causal, -1, stream);
+}
+
+ATTN_API int attn_debug_prefill_stall(const void* Q, const void* K, const void* V, void* O, int B,
+                                      int S, int H_q, int H_kv, int D, int causal, int stall_tile,
+                                      cudaStream_t stream)
+{
+    if (stall_tile < 0)
+        return ATTN_ERR_INVALID_ARG;
+    return prefill_checked(Q, K, V, O, B, S, H_q, H_kv, D, causal, stall_tile, stream);
 }
 
 ATTN_API size_t attn_decode_paged_workspace_bytes(int num_seqs, int H_q, int H_kv, int D,

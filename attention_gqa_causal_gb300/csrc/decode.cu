@@ -288,20 +288,27 @@ decode_splitk_kernel(const __half* __restrict__ q, const __half* __restrict__ k_
     }
 }
 
-// One warp per output row; lane owns 4 consecutive head-dim entries.
+// One CTA of kCombineWarps warps per output row; lane owns 4 consecutive
+// head-dim entries.  The warps take the row's splits round-robin (loads
+// unrolled for memory-level parallelism) and are merged in shared memory.
 // If seq_lens is given, row r = n*H_q + h uses the first
 // ceil(ceil(seq_lens[n]/16)/pages_per_split) partials; otherwise all n_split
 // (partials with lse = -inf contribute nothing).
-__global__ void __launch_bounds__(256)
+constexpr int kCombineWarps = 4;
+
+__global__ void __launch_bounds__(kCombineWarps * 32)
 lse_combine_kernel(const float* __restrict__ O_part, const float* __restrict__ lse_part,
-                   __half* __restrict__ out, int R, int n_split, const int* __restrict__ seq_lens,
+                   __half* __restrict__ out, int n_split, const int* __restrict__ seq_lens,
                    int H_q, int pages_per_split, int max_len)
 {
     constexpr int D = kHeadDim;
-    const int row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    constexpr int W = kCombineWarps;
+    __shared__ float sm_max[W];
+    __shared__ float sm_sum[W];
+    __shared__ float4 sm_acc[W][32];
+    const int row = blockIdx.x;
+    const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    if (row >= R)
-        return;
     int ns = n_split;
     if (seq_lens) {
         const int L = min(seq_lens[row / H_q], max_len);
@@ -309,32 +316,71 @@ lse_combine_kernel(const float* __restrict__ O_part, const float* __restrict__ l
         ns = (pages + pages_per_split - 1) / pages_per_split;
     }
     const float* lp = lse_part + (size_t)row * n_split;
+    const float* op = O_part + (size_t)row * n_split * D + lane * 4;
     float M = -CUDART_INF_F;
-    for (int i = lane; i < ns; i += 32)
+    for (int i = threadIdx.x; i < ns; i += W * 32)
         M = fmaxf(M, lp[i]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
         M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    if (lane == 0)
+        sm_max[warp] = M;
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < W; ++k)
+        M = fmaxf(M, sm_max[k]);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float wsum = 0.f;
     if (M != -CUDART_INF_F) {
-        float wsum = 0.f;
-        for (int i = 0; i < ns; ++i) {
-            const float w = ex2_approx((lp[i] - M) * kLog2e);
-            const float4 v = *reinterpret_cast<const float4*>(O_part + ((size_t)row * n_split + i) * D + lane * 4);
+        const float Ml = M * kLog2e;
+        int i = warp;
+        for (; i + 3 * W < ns; i += 4 * W) {
+            float wt[4];
+            float4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                wt[u] = lp[i + u * W];
+                v[u] = *reinterpret_cast<const float4*>(op + (size_t)(i + u * W) * D);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float w = ex2_approx(fmaf(wt[u], kLog2e, -Ml));
+                wsum += w;
+                acc.x = fmaf(w, v[u].x, acc.x);
+                acc.y = fmaf(w, v[u].y, acc.y);
+                acc.z = fmaf(w, v[u].z, acc.z);
+                acc.w = fmaf(w, v[u].w, acc.w);
+            }
+        }
+        for (; i < ns; i += W) {
+            const float w = ex2_approx(fmaf(lp[i], kLog2e, -Ml));
+            const float4 v = *reinterpret_cast<const float4*>(op + (size_t)i * D);
             wsum += w;
             acc.x = fmaf(w, v.x, acc.x);
             acc.y = fmaf(w, v.y, acc.y);
             acc.z = fmaf(w, v.z, acc.z);
             acc.w = fmaf(w, v.w, acc.w);
         }
-        const float inv = 1.f / wsum;
-        acc.x *= inv;
-        acc.y *= inv;
-        acc.z *= inv;
-        acc.w *= inv;
     }
-    __half2 h[2] = {__floats2half2_rn(acc.x, acc.y), __floats2half2_rn(acc.z, acc.w)};
-    *reinterpret_cast<uint2*>(out + (size_t)row * D + lane * 4) = *reinterpret_cast<uint2*>(h);
+    sm_acc[warp][lane] = acc;
+    if (lane == 0)
+        sm_sum[warp] = wsum;
+    __syncthreads();
+    if (warp == 0) {
+        float tot = 0.f;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+            tot += sm_sum[k];
+            a.x += sm_acc[k][lane].x;
+            a.y += sm_acc[k][lane].y;
+            a.z += sm_acc[k][lane].z;
+            a.w += sm_acc[k][lane].w;
+        }
+        const float inv = tot > 0.f ? 1.f / tot : 0.f;  // all segments empty -> zeros
+        __half2 h[2] = {__floats2half2_rn(a.x * inv, a.y * inv), __floats2half2_rn(a.z * inv, a.w * inv)};
+        *reinterpret_cast<uint2*>(out + (size_t)row * D + lane * 4) = *reinterpret_cast<uint2*>(h);
+    }
 }
 
 int pick_heads_per_cta(int group)
@@ -359,8 +405,17 @@ DecodePlan make_decode_plan(int num_seqs, int H_q, int H_kv, int max_blocks_per_
     p.group = H_q / H_kv;
     p.heads_per_cta = pick_heads_per_cta(p.group);
     p.chunks = (p.group + p.heads_per_cta - 1) / p.heads_per_cta;
-    if (pages_per_split <= 0)
-        pages_per_split = 16;
+    if (pages_per_split <= 0) {
+        // 32 pages (512 tokens) per split measured best on both decode
+        // workloads; smaller splits only when the grid would otherwise hold
+        // fewer than 16 CTAs per SM of a 152-SM GB300.
+        constexpr long long kTargetCtas = 16 * 152;
+        const long long units = (long long)num_seqs * H_kv * p.chunks;
+        pages_per_split = 32;
+        while (pages_per_split > 4 &&
+               units * ((max_blocks_per_seq + pages_per_split - 1) / pages_per_split) < kTargetCtas)
+            pages_per_split /= 2;
+    }
     p.pages_per_split = pages_per_split;
     p.n_split = (max_blocks_per_seq + pages_per_split - 1) / pages_per_split;
     const size_t rows = (size_t)num_seqs * H_q;
@@ -408,9 +463,8 @@ cudaError_t launch_decode(const DecodePlan& p, const void* q, const void* k_cach
     if (e != cudaSuccess)
         return e;
     const int R = p.num_seqs * p.H_q;
-    const int rows_per_block = 8;
-    lse_combine_kernel<<<(R + rows_per_block - 1) / rows_per_block, rows_per_block * 32, 0, stream>>>(
-        O_part, lse_part, static_cast<__half*>(out), R, p.n_split, seq_lens, p.H_q,
+    lse_combine_kernel<<<R, kCombineWarps * 32, 0, stream>>>(
+        O_part, lse_part, static_cast<__half*>(out), p.n_split, seq_lens, p.H_q,
         p.pages_per_split, p.max_blocks_per_seq * kPageSize);
     return cudaGetLastError();
 }
@@ -418,9 +472,8 @@ cudaError_t launch_decode(const DecodePlan& p, const void* q, const void* k_cach
 cudaError_t launch_lse_combine(const float* O_part, const float* lse_part, void* out, int R,
                                int n_split, cudaStream_t stream)
 {
-    const int rows_per_block = 8;
-    lse_combine_kernel<<<(R + rows_per_block - 1) / rows_per_block, rows_per_block * 32, 0, stream>>>(
-        O_part, lse_part, static_cast<__half*>(out), R, n_split, nullptr, 1, 1, 0);
+    lse_combine_kernel<<<R, kCombineWarps * 32, 0, stream>>>(
+        O_part, lse_part, static_cast<__half*>(out), n_split, nullptr, 1, 1, 0);
     return cudaGetLastError();
 }
 

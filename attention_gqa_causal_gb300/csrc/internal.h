@@ -53,7 +53,9 @@ cudaError_t launch_lse_combine(const float* O_part, const float* lse_part, void*
 int record_cuda_error(cudaError_t e);
 
 // Prefill: O = softmax(Q K^T / sqrt(D), causal) V over [B,S,H,D] tensors.
+// stall_tile >= 0 (failure-detection tests only) withholds that key tile's K
+// load in every CTA, so the waits on it run out and report a timeout.
 cudaError_t launch_prefill(const void* Q, const void* K, const void* V, void* O, int B, int S,
-                           int H_q, int H_kv, int causal, cudaStream_t stream);
+                           int H_q, int H_kv, int causal, int stall_tile, cudaStream_t stream);
 
 }  // namespace attn

@@ -81,6 +81,7 @@ struct PrefillArgs {
     int n_mb;           // number of row blocks
     int causal;
     float scale_log2;   // log2(e) / sqrt(D)
+    int stall_tile;     // failure-detection test only: key tile whose K load is withheld (-1: none)
 };
 
 struct Unit {
@@ -232,10 +233,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 if (!ok)
                     break;
                 const uint32_t kbar = smem_u32(&ctl.k_full[sk]);
-                mbar_arrive_expect_tx(kbar, kTileBytes);
-                for (int h = 0; h < 2; ++h)
-                    tma_load_4d(sbase + kSmemK + sk * kTileBytes + h * kBoxBytes, &tmK, kbar,
-                                h * 64, w.g, j * BN, w.b);
+                if (j != a.stall_tile) {
+                    mbar_arrive_expect_tx(kbar, kTileBytes);
+                    for (int h = 0; h < 2; ++h)
+                        tma_load_4d(sbase + kSmemK + sk * kTileBytes + h * kBoxBytes, &tmK, kbar,
+                                    h * 64, w.g, j * BN, w.b);
+                }
                 ++n_k;
                 const int sv = j % kVStages;
                 ok = mbar_wait(smem_u32(&ctl.v_empty[sv]), ((j / kVStages) & 1) ^ 1, abort);
@@ -255,8 +258,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             const int no_abort = 0;
             mbar_wait(qbar, 0, &no_abort);
             for (int s = 0; s < kKStages; ++s) {
-                // loads issued into stage s: tiles j < n_k with j % kKStages == s
-                const int c = n_k > s ? (n_k - s + kKStages - 1) / kKStages : 0;
+                // loads issued into stage s: tiles j < n_k with j % kKStages == s,
+                // except a withheld one
+                const int c = (n_k > s ? (n_k - s + kKStages - 1) / kKStages : 0) -
+                              ((a.stall_tile >= 0 && a.stall_tile < n_k && a.stall_tile % kKStages == s) ? 1 : 0);
                 if (c)
                     mbar_wait(smem_u32(&ctl.k_full[s]), (c - 1) & 1, &no_abort);
             }
@@ -527,7 +532,7 @@ bool make_bshd_map(CUtensorMap* m, const void* ptr, int B, int S, int H)
 }  // namespace
 
 cudaError_t launch_prefill(const void* Q, const void* K, const void* V, void* O, int B, int S,
-                           int H_q, int H_kv, int causal, cudaStream_t stream)
+                           int H_q, int H_kv, int causal, int stall_tile, cudaStream_t stream)
 {
     // the shared-memory opt-in is a per-device attribute
     static std::mutex attr_mutex;
@@ -568,6 +573,7 @@ cudaError_t launch_prefill(const void* Q, const void* K, const void* V, void* O,
     a.units_per_mb = B * H_kv * pairs_per_g;
     a.causal = causal ? 1 : 0;
     a.scale_log2 = kLog2e / sqrtf((float)D);
+    a.stall_tile = stall_tile;
     const long long grid = (long long)a.units_per_mb * a.n_mb;
     if (grid > 0x7fffffffLL)
         return cudaErrorInvalidConfiguration;

@@ -59,6 +59,20 @@ ATTN_API int attn_prefill(const void* Q, const void* K, const void* V, void* O, 
                           int H_q, int H_kv, int D, int causal, cudaStream_t stream);
 
 /*
+ * Failure-detection test hook (not for production use): attn_prefill, except
+ * that the K tile with index stall_tile (>= 0) is never loaded in any CTA
+ * that reaches it.  The on-chip waits for that tile run out after their
+ * ~1 s limit; every role of the kernel then leaves its loop, waits for its own
+ * copies and MMAs in flight, releases tensor memory and exits, and the device
+ * error word reports a timeout (attn_get_device_error -> ATTN_ERR_TIMEOUT).
+ * O is left unspecified for the affected rows.  Lets a test exercise the
+ * timeout path of the real kernel without faulting or hanging the GPU.
+ */
+ATTN_API int attn_debug_prefill_stall(const void* Q, const void* K, const void* V, void* O, int B,
+                                      int S, int H_q, int H_kv, int D, int causal, int stall_tile,
+                                      cudaStream_t stream);
+
+/*
  * Single-token decode over a paged KV cache.
  * Operation: same page, "Paged Attention -- Decode":
  *   out[n,h,:] = sum_{t < seq_lens[n]} softmax_t(q[n,h,:].K_t / sqrt(D)) V_t,
@@ -88,7 +102,8 @@ ATTN_API int attn_decode_paged(const void* q, const void* k_cache, const void* v
 
 /*
  * Bytes of scratch attn_decode_paged_ws needs for these sizes.
- * pages_per_split: KV pages per split-K work unit (<= 0 picks the default, 16).
+ * pages_per_split: KV pages per split-K work unit.  <= 0 picks the default: 32,
+ * halved (down to 4) while the grid would hold fewer than 2432 CTAs.
  * Returns 0 for invalid sizes.
  */
 ATTN_API size_t attn_decode_paged_workspace_bytes(int num_seqs, int H_q, int H_kv, int D,
