@@ -22,7 +22,9 @@ from ._binding import (  # noqa: F401
     AttnError,
     attn_debug_prefill_stall,
     attn_decode_paged,
+    attn_decode_paged_append,
     attn_decode_paged_noalloc,
+    attn_kv_append,
     attn_decode_paged_workspace_bytes,
     attn_decode_paged_ws,
     attn_get_device_error,

@@ -26,7 +26,8 @@ EXPORTED = [
     "attn_prefill", "attn_decode_paged", "attn_decode_paged_workspace_bytes",
     "attn_decode_paged_ws", "attn_lse_combine", "attn_release_workspace",
     "attn_get_device_error", "attn_last_cuda_error", "attn_status_string", "attn_version",
-    "attn_decode_paged_noalloc", "attn_debug_prefill_stall",
+    "attn_decode_paged_noalloc", "attn_debug_prefill_stall", "attn_kv_append",
+    "attn_decode_paged_append",
 ]
 
 # Size of the scratch buffer compiled into the library for attn_decode_paged_noalloc.
@@ -67,6 +68,10 @@ def load():
             lib.attn_version.argtypes = []
             lib.attn_decode_paged_noalloc.argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, p]
             lib.attn_debug_prefill_stall.argtypes = [p, p, p, p, i, i, i, i, i, i, i, p]
+            ll = ctypes.c_longlong
+            lib.attn_kv_append.argtypes = [p, p, p, p, p, i, i, i, i, ll, p]
+            lib.attn_decode_paged_append.argtypes = [p, p, p, p, p, p, p, p, p, i, i, i, i, i, i,
+                                                     ll, p]
             _lib = lib
     return _lib
 
@@ -146,6 +151,37 @@ def attn_decode_paged(q, k_cache, v_cache, out, block_tables, seq_lens, stream=N
     ptrs, sizes = _decode_args(q, k_cache, v_cache, out, block_tables, seq_lens)
     st = _stream(stream, q.device)
     _check(load().attn_decode_paged(*ptrs, *sizes, ctypes.c_void_p(st)), "attn_decode_paged")
+
+
+def attn_kv_append(k_new, v_new, k_cache, v_cache, slot_mapping, stream=None) -> None:
+    """Write new K/V rows [T, H_kv, D] into their paged slots (int64 slot_mapping, -1 skips)."""
+    if k_new.dim() != 3 or v_new.shape != k_new.shape or k_cache.dim() != 4 or v_cache.shape != k_cache.shape:
+        raise ValueError("expected k_new/v_new [T,H_kv,D] and caches [num_blocks,H_kv,block_size,D]")
+    T, H_kv, D = k_new.shape
+    if slot_mapping.shape != (T,):
+        raise ValueError("expected slot_mapping [T]")
+    ptrs = [_dev(k_new, "k_new", torch.float16), _dev(v_new, "v_new", torch.float16),
+            _dev(k_cache, "k_cache", torch.float16), _dev(v_cache, "v_cache", torch.float16),
+            _dev(slot_mapping, "slot_mapping", torch.int64)]
+    st = _stream(stream, k_new.device)
+    _check(load().attn_kv_append(*ptrs, T, H_kv, D, k_cache.shape[2], k_cache.shape[0],
+                                 ctypes.c_void_p(st)), "attn_kv_append")
+
+
+def attn_decode_paged_append(q, k_new, v_new, k_cache, v_cache, out, slot_mapping, block_tables,
+                             seq_lens, stream=None) -> None:
+    """One decode step: append each sequence's new K/V row, then paged decode."""
+    ptrs, sizes = _decode_args(q, k_cache, v_cache, out, block_tables, seq_lens)
+    N = q.shape[0]
+    if k_new.shape != (N, k_cache.shape[1], q.shape[2]) or v_new.shape != k_new.shape or slot_mapping.shape != (N,):
+        raise ValueError("expected k_new/v_new [N,H_kv,D] and slot_mapping [N]")
+    extra = [_dev(k_new, "k_new", torch.float16), _dev(v_new, "v_new", torch.float16),
+             _dev(slot_mapping, "slot_mapping", torch.int64)]
+    st = _stream(stream, q.device)
+    # C order: q, k_new, v_new, k_cache, v_cache, out, slot_mapping, block_tables, seq_lens
+    _check(load().attn_decode_paged_append(ptrs[0], extra[0], extra[1], ptrs[1], ptrs[2], ptrs[3],
+                                           extra[2], ptrs[4], ptrs[5], *sizes, k_cache.shape[0],
+                                           ctypes.c_void_p(st)), "attn_decode_paged_append")
 
 
 def attn_decode_paged_workspace_bytes(num_seqs: int, H_q: int, H_kv: int, D: int,

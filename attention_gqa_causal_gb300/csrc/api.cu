@@ -189,6 +189,50 @@ ATTN_API int attn_decode_paged(const void* q, const void* k_cache, const void* v
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
 
+ATTN_API int attn_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                            const long long* slot_mapping, int num_tokens, int H_kv, int D,
+                            int block_size, long long num_blocks, cudaStream_t stream)
+{
+    if (num_tokens < 0 || H_kv < 1 || num_blocks < 0)
+        return ATTN_ERR_INVALID_ARG;
+    if (D != attn::kHeadDim || block_size != attn::kPageSize)
+        return ATTN_ERR_UNSUPPORTED;
+    if (num_tokens == 0)
+        return ATTN_OK;
+    if (!k_new || !v_new || !k_cache || !v_cache || !slot_mapping || !aligned(k_new, 16) ||
+        !aligned(v_new, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(slot_mapping, 8))
+        return ATTN_ERR_INVALID_ARG;
+    const size_t new_bytes = (size_t)num_tokens * H_kv * D * 2;
+    const size_t cache_bytes = (size_t)num_blocks * H_kv * block_size * D * 2;
+    if (overlap(k_cache, cache_bytes, k_new, new_bytes) || overlap(k_cache, cache_bytes, v_new, new_bytes) ||
+        overlap(v_cache, cache_bytes, k_new, new_bytes) || overlap(v_cache, cache_bytes, v_new, new_bytes) ||
+        overlap(k_cache, cache_bytes, v_cache, cache_bytes))
+        return ATTN_ERR_INVALID_ARG;
+    const cudaError_t e = attn::launch_kv_append(k_new, v_new, k_cache, v_cache, slot_mapping,
+                                                 num_tokens, H_kv, num_blocks, stream);
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+ATTN_API int attn_decode_paged_append(const void* q, const void* k_new, const void* v_new,
+                                      void* k_cache, void* v_cache, void* out,
+                                      const long long* slot_mapping, const int* block_tables,
+                                      const int* seq_lens, int num_seqs, int H_q, int H_kv, int D,
+                                      int max_blocks_per_seq, int block_size, long long num_blocks,
+                                      cudaStream_t stream)
+{
+    const int v = validate_decode(q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q,
+                                  H_kv, D, max_blocks_per_seq, block_size);
+    if (v != ATTN_OK || num_seqs == 0)
+        return v;
+    const int r = attn_kv_append(k_new, v_new, k_cache, v_cache, slot_mapping, num_seqs, H_kv, D,
+                                 block_size, num_blocks, stream);
+    if (r != ATTN_OK)
+        return r;
+    return attn_decode_paged(q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
+                             D, max_blocks_per_seq, block_size, stream);
+}
+
 ATTN_API int attn_lse_combine(const float* O_part, const float* lse, void* out, int R,
                               int n_split, int D, cudaStream_t stream)
 {

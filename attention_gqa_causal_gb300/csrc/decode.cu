@@ -477,4 +477,49 @@ cudaError_t launch_lse_combine(const float* O_part, const float* lse_part, void*
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ KV append
+//
+// "GRPO-CUDA Project Memory" page, "KV Cache design": reshape-and-cache
+// writes each new token's K/V row into its paged slot, slot_mapping[token] =
+// physical_block * block_size + offset (int64), and skips slot -1 (padding
+// tokens, "Known bugs fixed").  One CTA per token; 16-byte copies of the
+// token's H_kv head rows of K and of V.  Slots outside [0, num_blocks*16)
+// other than -1 are skipped and flagged.
+
+__global__ void __launch_bounds__(128)
+kv_append_kernel(const __half* __restrict__ k_new, const __half* __restrict__ v_new,
+                 __half* __restrict__ k_cache, __half* __restrict__ v_cache,
+                 const long long* __restrict__ slot_mapping, int H_kv, long long num_blocks)
+{
+    constexpr int D = kHeadDim;
+    constexpr int BS = kPageSize;
+    const int t = blockIdx.x;
+    const long long slot = slot_mapping[t];
+    if (slot < 0 || slot >= num_blocks * BS) {
+        if (slot != -1 && threadIdx.x == 0)
+            atomicOr(&g_device_error, kDevErrBadSlot);
+        return;
+    }
+    const long long block = slot / BS;
+    const int pos = (int)(slot % BS);
+    const int chunks = H_kv * D / 8;  // 16-byte chunks per row set
+    for (int c = threadIdx.x; c < chunks; c += blockDim.x) {
+        const int g = c / (D / 8), d8 = c % (D / 8);
+        const size_t src = ((size_t)t * H_kv + g) * D + d8 * 8;
+        const size_t dst = (((size_t)block * H_kv + g) * BS + pos) * D + d8 * 8;
+        *reinterpret_cast<uint4*>(k_cache + dst) = *reinterpret_cast<const uint4*>(k_new + src);
+        *reinterpret_cast<uint4*>(v_cache + dst) = *reinterpret_cast<const uint4*>(v_new + src);
+    }
+}
+
+cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                             const long long* slot_mapping, int num_tokens, int H_kv,
+                             long long num_blocks, cudaStream_t stream)
+{
+    kv_append_kernel<<<num_tokens, 128, 0, stream>>>(
+        static_cast<const __half*>(k_new), static_cast<const __half*>(v_new),
+        static_cast<__half*>(k_cache), static_cast<__half*>(v_cache), slot_mapping, H_kv, num_blocks);
+    return cudaGetLastError();
+}
+
 }  // namespace attn

@@ -17,6 +17,7 @@ enum DeviceError : int {
     kDevErrSeqTooLong = 4,     // seq_lens[n] > max_blocks_per_seq * block_size
     kDevErrTmemAlloc = 8,      // TMEM base address outside the expected range
     kDevErrSmemLayout = 16,    // dynamic shared memory base too misaligned for the tile layout
+    kDevErrBadSlot = 32,       // a slot_mapping entry outside [-1, num_blocks * block_size)
 };
 
 // Set by the kernels (atomicOr); defined in decode.cu.  Device address of the
@@ -45,6 +46,12 @@ cudaError_t launch_decode(const DecodePlan& p, const void* q, const void* k_cach
                           const int* seq_lens, void* ws, cudaStream_t stream);
 
 // Merge R rows of n_split partials (O normalised per split, lse natural log).
+// Write num_tokens new K/V rows ([num_tokens, H_kv, 128] each) into their
+// paged slots: slot s -> block s / 16, position s % 16; s == -1 is skipped.
+cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                             const long long* slot_mapping, int num_tokens, int H_kv,
+                             long long num_blocks, cudaStream_t stream);
+
 cudaError_t launch_lse_combine(const float* O_part, const float* lse_part, void* out, int R,
                                int n_split, cudaStream_t stream);
 

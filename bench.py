@@ -7,6 +7,7 @@ One step is one pass over every hot-path kernel on its workload:
   * the same shape without the mask (the unmasked tensor-core ceiling)
   * paged decode          256 sequences, lengths uniform on [128, 2048], H 16/8
   * paged decode          8 sequences x 32768 tokens, H 16/8
+  * the 256-sequence decode step together with its KV append (two launches)
     (decode: GB/s of K/V bytes of the valid tokens; split-K + combine kernels)
 Each kernel launch is bracketed by CUDA events on the stream it runs on; the
 K timed steps are bracketed by a barrier and a device synchronisation.  All
@@ -169,7 +170,7 @@ def build_legs(torch, ag, which):
                           "causal": cfg.causal}
             legs.append(leg)
     for cfg, key in ((W.DECODE_MIX, "decode"), (W.DECODE_LONG, "decode_long")):
-        if which not in ("all", key):
+        if which not in ("all", key) and not (key == "decode" and which == "decode_append"):
             continue
         inp = W.decode_inputs(cfg, seed=0)
         t = [torch.from_numpy(x).cuda() for x in (inp.q, inp.k_cache, inp.v_cache,
@@ -184,7 +185,25 @@ def build_legs(torch, ag, which):
                       "block_size": cfg.block_size, "seq_len": [cfg.len_lo, cfg.len_hi],
                       "max_blocks_per_seq": cfg.max_blocks_per_seq,
                       "num_blocks": inp.num_blocks, "kv_bytes": inp.kv_bytes()}
-        legs.append(leg)
+        if which != "decode_append":
+            legs.append(leg)
+        if cfg is W.DECODE_MIX and which in ("all", "decode_append"):
+            # one decode step with its KV append: each sequence's new token goes to
+            # its last position (rewritten every step, so steps are idempotent)
+            N, H_kv = cfg.num_seqs, cfg.H_kv
+            Ls = inp.seq_lens.astype(np.int64)
+            slots = inp.block_tables[np.arange(N), (Ls - 1) // 16].astype(np.int64) * 16 + (Ls - 1) % 16
+            kn = W.normal_fp16(0, 7, (N, H_kv, cfg.D))
+            vn = W.normal_fp16(0, 8, (N, H_kv, cfg.D))
+            dkn, dvn, dsl = (torch.from_numpy(x).cuda() for x in (kn, vn, slots))
+            app_bytes = 2 * kn.nbytes
+            leg2 = Leg(cfg.name + "_append", "decode", float(inp.kv_bytes() + app_bytes), "GB/s", 3)
+            leg2.run = (lambda t=t, out=out, dkn=dkn, dvn=dvn, dsl=dsl: ag.attn_decode_paged_append(
+                t[0], dkn, dvn, t[1], t[2], out, dsl, t[3], t[4]))
+            leg2.host = dict(leg.host, k_new=kn, v_new=vn, slot_mapping=slots)
+            leg2.dev_in, leg2.dev_out = tuple(t) + (dkn, dvn, dsl), out
+            leg2.config = dict(leg.config, append_bytes=app_bytes)
+            legs.append(leg2)
     return legs
 
 
@@ -391,7 +410,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["all", "prefill", "prefill_full", "decode", "decode_long"],
+    ap.add_argument("--workload", choices=["all", "prefill", "prefill_full", "decode", "decode_long",
+                                           "decode_append"],
                     default="all")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="CPU time budget of the oracle baseline sample")

@@ -40,7 +40,7 @@ enum {
     ATTN_ERR_UNSUPPORTED = -2,  /* head_dim != 128 or block_size != 16 */
     ATTN_ERR_CUDA = -3,         /* a CUDA runtime call failed; see attn_last_cuda_error() */
     ATTN_ERR_TIMEOUT = -4,      /* device error word: a bounded on-chip wait gave up */
-    ATTN_ERR_BAD_INPUT = -5,    /* device error word: negative block id or seq_len beyond the table */
+    ATTN_ERR_BAD_INPUT = -5,    /* device error word: negative block id, seq_len beyond the table, slot out of range */
     ATTN_ERR_WORKSPACE = -6     /* caller workspace missing or smaller than required */
 };
 
@@ -152,6 +152,38 @@ ATTN_API int attn_decode_paged_noalloc(const void* q, const void* k_cache, const
                                        cudaStream_t stream);
 
 /*
+ * Append new tokens' K and V rows to the paged cache ("GRPO-CUDA Project
+ * Memory" page, "KV Cache design": reshape-and-cache with
+ * slot_mapping[token] = physical_block * block_size + offset, int64; slot -1
+ * is a padding token and is skipped, "Known bugs fixed").
+ * k_new, v_new : [num_tokens, H_kv, D] FP16
+ * k/v_cache    : [num_blocks, H_kv, block_size, D] FP16, updated in place
+ * slot_mapping : [num_tokens] int64 (8-byte aligned)
+ * D must be 128 and block_size 16.  A slot outside [-1, num_blocks*block_size)
+ * is skipped and flagged in the device error word (ATTN_ERR_BAD_INPUT).  Two
+ * tokens mapped to the same slot race (the last write wins, unspecified).
+ * The new rows must not overlap the caches.
+ */
+ATTN_API int attn_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                            const long long* slot_mapping, int num_tokens, int H_kv, int D,
+                            int block_size, long long num_blocks, cudaStream_t stream);
+
+/*
+ * One decode step with its KV append: attn_kv_append of one new token per
+ * sequence (k_new/v_new [num_seqs, H_kv, D], slot_mapping [num_seqs]) followed
+ * on the same stream by attn_decode_paged over the updated cache (seq_lens
+ * already counting the new token), as the page's layer order prescribes (KV
+ * append, then attention: "Model forward pass").  Two launches in one call;
+ * scratch as attn_decode_paged.
+ */
+ATTN_API int attn_decode_paged_append(const void* q, const void* k_new, const void* v_new,
+                                      void* k_cache, void* v_cache, void* out,
+                                      const long long* slot_mapping, const int* block_tables,
+                                      const int* seq_lens, int num_seqs, int H_q, int H_kv, int D,
+                                      int max_blocks_per_seq, int block_size, long long num_blocks,
+                                      cudaStream_t stream);
+
+/*
  * Merge partial attention results over disjoint key segments by their
  * log-sum-exp (the combine step of split-K decode):
  *   L = log sum_i exp(lse[r,i]),  out[r,:] = sum_i exp(lse[r,i] - L) O_part[r,i,:]
@@ -170,7 +202,8 @@ ATTN_API int attn_release_workspace(void);
 /*
  * Read the device error word of the current device (synchronises the device).
  * *code receives the raw bits (1 timeout, 2 negative block id, 4 seq_len
- * beyond the table); the return is ATTN_OK if it is 0, else ATTN_ERR_TIMEOUT
+ * beyond the table, 16 shared-memory layout did not fit, 32 slot out of
+ * range); the return is ATTN_OK if it is 0, else ATTN_ERR_TIMEOUT
  * or ATTN_ERR_BAD_INPUT.  reset != 0 clears it.
  */
 ATTN_API int attn_get_device_error(int* code, int reset);

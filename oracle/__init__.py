@@ -191,3 +191,18 @@ def variant(lib_path: str):
         yield
     finally:
         _lib = saved
+
+
+def kv_append(k_new, v_new, k_cache, v_cache, slot_mapping):
+    """Return copies of the caches with the new rows written to their slots
+    (int64 slot_mapping, -1 skipped) and the count of out-of-range slots."""
+    k_new, v_new = _half(k_new), _half(v_new)
+    kc, vc = _half(k_cache).copy(), _half(v_cache).copy()
+    sm = np.ascontiguousarray(slot_mapping, np.int64)
+    T, H_kv, D = k_new.shape
+    lib = _load()
+    lib.oracle_kv_append.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int] * 4 + [ctypes.c_long]
+    lib.oracle_kv_append.restype = ctypes.c_int
+    bad = lib.oracle_kv_append(_ptr(k_new), _ptr(v_new), _ptr(kc), _ptr(vc), _ptr(sm), T, H_kv, D,
+                               kc.shape[2], kc.shape[0])
+    return kc, vc, int(bad)

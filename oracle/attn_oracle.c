@@ -340,3 +340,35 @@ void oracle_lse_combine(const double *O_part, const double *lse_part, int R, int
             lse[r] = L;
     }
 }
+
+/*
+ * Write new K/V rows into their paged slots ("GRPO-CUDA Project Memory" page,
+ * "KV Cache design": slot = physical_block * block_size + offset; slot -1 is a
+ * padding token and is skipped).  Raw 16-bit copies, so the result is exact.
+ * k_new, v_new: [T, H_kv, D]; caches: [num_blocks, H_kv, bs, D] updated in place.
+ * Slots outside [0, num_blocks*bs) are skipped; returns how many were.
+ */
+int oracle_kv_append(const uint16_t *k_new, const uint16_t *v_new, uint16_t *k_cache,
+                     uint16_t *v_cache, const int64_t *slot_mapping, int T, int H_kv, int D,
+                     int bs, long num_blocks)
+{
+    int skipped = 0;
+    for (int t = 0; t < T; t++) {
+        const int64_t slot = slot_mapping[t];
+        if (slot < 0 || slot >= (int64_t)num_blocks * bs) {
+            if (slot != -1)
+                skipped++;
+            continue;
+        }
+        const long block = (long)(slot / bs);
+        const int pos = (int)(slot % bs);
+        for (int g = 0; g < H_kv; g++)
+            for (int d = 0; d < D; d++) {
+                const long dst = (((block * H_kv) + g) * bs + pos) * (long)D + d;
+                const long src = ((long)t * H_kv + g) * (long)D + d;
+                k_cache[dst] = k_new[src];
+                v_cache[dst] = v_new[src];
+            }
+    }
+    return skipped;
+}

@@ -124,3 +124,20 @@ def test_binding_rejects_cpu_tensors():
     x = torch.zeros(1, 4, 2, 128, dtype=torch.float16)
     with pytest.raises(ValueError):
         ag.attn_prefill(x, x[:, :, :1], x[:, :, :1], x.clone())
+
+
+def test_kv_append_validation():
+    lib = ag.load()
+    LL = ctypes.c_longlong
+
+    def app(kn=A16, vn=A16 + 0x10000, kc=A16B, vc=A16B + 0x1000000, sm=A16 + 0x20000, T=4, Hkv=8, D=128,
+            bs=16, nb=16):
+        return lib.attn_kv_append(P(kn), P(vn), P(kc), P(vc), P(sm), T, Hkv, D, bs, LL(nb), P(0))
+
+    assert app(D=64) == ag.ATTN_ERR_UNSUPPORTED
+    assert app(bs=8) == ag.ATTN_ERR_UNSUPPORTED
+    assert app(T=-1) == ag.ATTN_ERR_INVALID_ARG
+    assert app(sm=A16 + 0x20004) == ag.ATTN_ERR_INVALID_ARG      # slot_mapping must be 8-byte aligned
+    assert app(kn=0) == ag.ATTN_ERR_INVALID_ARG
+    assert app(kc=A16) == ag.ATTN_ERR_INVALID_ARG                # cache overlaps the new rows
+    assert app(T=0) == ag.ATTN_OK

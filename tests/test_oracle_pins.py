@@ -297,3 +297,21 @@ def test_lse_merge_two_known_partials():
     wa = math.exp(a) / (math.exp(a) + math.exp(b))
     np.testing.assert_allclose(out[0], [wa, 1 - wa], atol=1e-15)
     assert abs(lse[0] - math.log(math.exp(a) + math.exp(b))) < 1e-15
+
+
+def test_kv_append_matches_fancy_indexing_scatter():
+    rng = np.random.default_rng(40)
+    nb, H_kv, bs, D, T = 7, 3, 16, 8, 9
+    kc, vc = _rand16(rng, (nb, H_kv, bs, D)), _rand16(rng, (nb, H_kv, bs, D))
+    kn, vn = _rand16(rng, (T, H_kv, D)), _rand16(rng, (T, H_kv, D))
+    slots = rng.choice(nb * bs, size=T, replace=False).astype(np.int64)
+    slots[2] = -1                       # padding token: skipped
+    slots[5] = nb * bs + 3              # out of range: skipped and counted
+    k2, v2, bad = oracle.kv_append(kn, vn, kc, vc, slots)
+    assert bad == 1
+    ek, ev = kc.copy(), vc.copy()
+    ok = (slots >= 0) & (slots < nb * bs)
+    ek[slots[ok] // bs, :, slots[ok] % bs, :] = kn[ok]
+    ev[slots[ok] // bs, :, slots[ok] % bs, :] = vn[ok]
+    assert np.array_equal(k2.view(np.uint16), ek.view(np.uint16))
+    assert np.array_equal(v2.view(np.uint16), ev.view(np.uint16))
