@@ -206,3 +206,25 @@ def kv_append(k_new, v_new, k_cache, v_cache, slot_mapping):
     bad = lib.oracle_kv_append(_ptr(k_new), _ptr(v_new), _ptr(kc), _ptr(vc), _ptr(sm), T, H_kv, D,
                                kc.shape[2], kc.shape[0])
     return kc, vc, int(bad)
+
+
+def prefill_paged(Q, k_cache, v_cache, cu_seqlens_q, seq_lens_kv, block_tables, causal=True,
+                  with_lse=False):
+    """New query chunks (packed Q [total_q, H_q, D], cu_seqlens_q [B+1]) against
+    a paged cache holding L_kv = seq_lens_kv[b] keys per sequence, the last
+    L_q of them the chunk's own; query i sits at position L_kv - L_q + i."""
+    Q, kc, vc = _half(Q), _half(k_cache), _half(v_cache)
+    cu, sl, bt = _i32(cu_seqlens_q), _i32(seq_lens_kv), _i32(block_tables)
+    total_q, H_q, D = Q.shape
+    B = sl.shape[0]
+    assert cu.shape == (B + 1,) and cu[-1] == total_q
+    H_kv, bs = kc.shape[1], kc.shape[2]
+    O = np.empty((total_q, H_q, D), np.float64)
+    lse = np.empty((total_q, H_q), np.float64)
+    lib = _load()
+    p, i = ctypes.c_void_p, ctypes.c_int
+    lib.oracle_prefill_paged.argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, i, p, p]
+    lib.oracle_prefill_paged.restype = None
+    lib.oracle_prefill_paged(_ptr(Q), _ptr(kc), _ptr(vc), _ptr(cu), _ptr(sl), _ptr(bt), B, H_q,
+                             H_kv, D, bt.shape[1], bs, int(bool(causal)), _ptr(O), _ptr(lse))
+    return (O, lse) if with_lse else O

@@ -372,3 +372,55 @@ int oracle_kv_append(const uint16_t *k_new, const uint16_t *v_new, uint16_t *k_c
     }
     return skipped;
 }
+
+/*
+ * Prefill of new query chunks against a paged KV cache (varlen, with cached
+ * prefix).  Sequence b has L_q = cu_seqlens_q[b+1] - cu_seqlens_q[b] new
+ * queries, packed at rows cu_seqlens_q[b].. of Q and O ([total_q, H_q, D]),
+ * and a context of L_kv = seq_lens_kv[b] keys in the paged cache (its last
+ * L_q keys belong to the new queries, L_kv >= L_q).  Query i of sequence b
+ * sits at absolute position L_kv - L_q + i; with the causal mask it attends to
+ * keys t <= L_kv - L_q + i, otherwise to all L_kv keys.  The key placement is
+ * the paged layout of the "Paged Attention -- Decode" header; the causal rule
+ * is the prefill one, shifted by the cached prefix.
+ */
+void oracle_prefill_paged(const uint16_t *Q, const uint16_t *k_cache, const uint16_t *v_cache,
+                          const int32_t *cu_seqlens_q, const int32_t *seq_lens_kv,
+                          const int32_t *block_tables, int B, int H_q, int H_kv, int D,
+                          int max_blocks_per_seq, int block_size, int causal, double *O,
+                          double *lse)
+{
+    const int total_q = cu_seqlens_q[B];
+    const int L = max_len(seq_lens_kv, B);
+    const long rows = (long)total_q * H_q;
+#pragma omp parallel
+    {
+        double *scores = (double *)malloc(sizeof(double) * L);
+#pragma omp for schedule(dynamic, 4)
+        for (long r = 0; r < rows; r++) {
+            const int h = (int)(r % H_q);
+            const int row = (int)(r / H_q);
+            int b = 0;
+            while (cu_seqlens_q[b + 1] <= row)
+                b++;
+            const int i = row - cu_seqlens_q[b];
+            const int Lq = cu_seqlens_q[b + 1] - cu_seqlens_q[b];
+            const int Lkv = seq_lens_kv[b];
+            paged_ctx c;
+            c.kc = k_cache;
+            c.vc = v_cache;
+            c.table = block_tables + (long)b * max_blocks_per_seq;
+            c.H_kv = H_kv;
+            c.bs = block_size;
+            c.D = D;
+            c.g = (int)(((long)h * H_kv) / H_q);
+            const int n = causal ? Lkv - Lq + i + 1 : Lkv;
+            double l;
+            attend_one(Q + ((long)row * H_q + h) * D, D, n, paged_key, paged_val, &c, scores,
+                       O + r * D, &l);
+            if (lse)
+                lse[r] = l;
+        }
+        free(scores);
+    }
+}

@@ -21,6 +21,8 @@ MUTANTS = {
     "lse_missing_max": ("*lse = M + log(sum);", "*lse = log(sum);"),
     "combine_weight_by_max": ("const double w = exp(lp[i] - L);", "const double w = exp(lp[i] - M);"),
     "decode_gqa_map": ("c.g = (int)(((long)h * H_kv) / H_q);", "c.g = (int)(h % H_kv);"),
+    "paged_prefill_no_prefix_offset": ("const int n = causal ? Lkv - Lq + i + 1 : Lkv;",
+                                       "const int n = causal ? i + 1 : Lkv;"),
 }
 
 PINS = [
@@ -32,6 +34,7 @@ PINS = [
     pins.test_decode_matches_sdpa_on_gathered_keys_ragged,
     lambda: pins.test_lse_merge_of_segments_equals_whole([0, 1, 2, 33, 40]),
     pins.test_lse_merge_two_known_partials,
+    pins.test_prefill_paged_equals_last_rows_of_full_causal_prefill,
 ]
 
 

@@ -315,3 +315,64 @@ def test_kv_append_matches_fancy_indexing_scatter():
     ev[slots[ok] // bs, :, slots[ok] % bs, :] = vn[ok]
     assert np.array_equal(k2.view(np.uint16), ek.view(np.uint16))
     assert np.array_equal(v2.view(np.uint16), ev.view(np.uint16))
+
+
+# ---------------------------------------------------------- paged prefill
+
+def _paged_problem(rng, lens_kv, lens_q, H_q, H_kv, D, bs=16, nan_unused=True):
+    """Contiguous K/V per sequence, the same keys in a permuted paged cache
+    (unused slots NaN), and packed queries for the last lens_q positions."""
+    B = len(lens_kv)
+    K = [_rand16(rng, (L, H_kv, D)) for L in lens_kv]
+    V = [_rand16(rng, (L, H_kv, D)) for L in lens_kv]
+    pages = [(L + bs - 1) // bs for L in lens_kv]
+    nb = sum(pages)
+    perm = rng.permutation(nb).astype(np.int32)
+    mb = max(pages) + 1
+    kc = np.full((nb, H_kv, bs, D), np.nan if nan_unused else 0.0, np.float16)
+    vc = kc.copy()
+    table = np.full((B, mb), -1, np.int32)
+    off = 0
+    for b in range(B):
+        for p in range(pages[b]):
+            phys = perm[off + p]
+            table[b, p] = phys
+            t0, t1 = p * bs, min(lens_kv[b], (p + 1) * bs)
+            kc[phys, :, :t1 - t0] = K[b][t0:t1].transpose(1, 0, 2)
+            vc[phys, :, :t1 - t0] = V[b][t0:t1].transpose(1, 0, 2)
+        off += pages[b]
+    Qs = [_rand16(rng, (Lq, H_q, D)) for Lq in lens_q]
+    cu = np.concatenate([[0], np.cumsum(lens_q)]).astype(np.int32)
+    return K, V, kc, vc, table, np.concatenate(Qs), cu, np.array(lens_kv, np.int32)
+
+
+def test_prefill_paged_equals_last_rows_of_full_causal_prefill():
+    rng = np.random.default_rng(50)
+    lens_kv, lens_q, H_q, H_kv, D = [40, 17, 70], [9, 17, 1], 4, 2, 16
+    K, V, kc, vc, table, Q, cu, skv = _paged_problem(rng, lens_kv, lens_q, H_q, H_kv, D)
+    out = oracle.prefill_paged(Q, kc, vc, cu, skv, table, causal=True)
+    assert np.isfinite(out).all()           # NaN in unused slots never read
+    for b, (Lkv, Lq) in enumerate(zip(lens_kv, lens_q)):
+        # a full causal prefill of the whole sequence, whose last Lq query rows are the chunk
+        Qfull = _rand16(rng, (1, Lkv, H_q, D))
+        Qfull[0, Lkv - Lq:] = Q[cu[b]:cu[b + 1]]
+        ref = _sdpa(Qfull, K[b][None], V[b][None], causal=True)[0, Lkv - Lq:]
+        np.testing.assert_allclose(out[cu[b]:cu[b + 1]], ref, atol=1e-12)
+
+
+def test_prefill_paged_noncausal_and_decode_special_case():
+    rng = np.random.default_rng(51)
+    lens_kv, lens_q, H_q, H_kv, D = [33, 5], [1, 1], 8, 2, 32
+    K, V, kc, vc, table, Q, cu, skv = _paged_problem(rng, lens_kv, lens_q, H_q, H_kv, D)
+    # one new query per sequence: paged prefill == paged decode (causal or not)
+    for causal in (True, False):
+        out = oracle.prefill_paged(Q, kc, vc, cu, skv, table, causal=causal)
+        dec = oracle.decode_paged(Q, kc, vc, table, skv)
+        np.testing.assert_allclose(out, dec, atol=1e-14)
+    # non-causal chunk: every query sees all L_kv keys
+    lens_q2 = [6, 3]
+    K, V, kc, vc, table, Q, cu, skv = _paged_problem(rng, lens_kv, lens_q2, H_q, H_kv, D)
+    out = oracle.prefill_paged(Q, kc, vc, cu, skv, table, causal=False)
+    for b in range(2):
+        ref = _sdpa(Q[cu[b]:cu[b + 1]][None], K[b][None], V[b][None], causal=False)[0]
+        np.testing.assert_allclose(out[cu[b]:cu[b + 1]], ref, atol=1e-12)
