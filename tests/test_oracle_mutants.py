@@ -20,7 +20,8 @@ MUTANTS = {
     "page_slot_swapped": ("* x->bs + (t % x->bs)) * (long)x->D;", "* x->bs + (t / x->bs) % x->bs) * (long)x->D;"),
     "lse_missing_max": ("*lse = M + log(sum);", "*lse = log(sum);"),
     "combine_weight_by_max": ("const double w = exp(lp[i] - L);", "const double w = exp(lp[i] - M);"),
-    "decode_gqa_map": ("c.g = (int)(((long)h * H_kv) / H_q);", "c.g = (int)(h % H_kv);"),
+    "decode_gqa_map": ("c.g = (int)(((long)h * H_kv) / H_q);\n    attend_one(q + ((long)n * H_q + h) * D",
+                       "c.g = (int)(h % H_kv);\n    attend_one(q + ((long)n * H_q + h) * D"),
     "paged_prefill_no_prefix_offset": ("const int n = causal ? Lkv - Lq + i + 1 : Lkv;",
                                        "const int n = causal ? i + 1 : Lkv;"),
 }
