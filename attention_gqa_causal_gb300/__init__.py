@@ -30,6 +30,7 @@ from ._binding import (  # noqa: F401
     attn_get_device_error,
     attn_lse_combine,
     attn_prefill,
+    attn_prefill_paged,
     attn_release_workspace,
     attn_version,
     load,

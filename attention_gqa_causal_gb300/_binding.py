@@ -27,7 +27,7 @@ EXPORTED = [
     "attn_decode_paged_ws", "attn_lse_combine", "attn_release_workspace",
     "attn_get_device_error", "attn_last_cuda_error", "attn_status_string", "attn_version",
     "attn_decode_paged_noalloc", "attn_debug_prefill_stall", "attn_kv_append",
-    "attn_decode_paged_append",
+    "attn_decode_paged_append", "attn_prefill_paged",
 ]
 
 # Size of the scratch buffer compiled into the library for attn_decode_paged_noalloc.
@@ -72,6 +72,7 @@ def load():
             lib.attn_kv_append.argtypes = [p, p, p, p, p, i, i, i, i, ll, p]
             lib.attn_decode_paged_append.argtypes = [p, p, p, p, p, p, p, p, p, i, i, i, i, i, i,
                                                      ll, p]
+            lib.attn_prefill_paged.argtypes = [p, p, p, p, p, p, p, i, i, i, i, i, i, i, i, ll, i, p]
             _lib = lib
     return _lib
 
@@ -118,6 +119,27 @@ def attn_prefill(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.Ten
     st = _stream(stream, Q.device)
     _check(load().attn_prefill(*args, B, S, H_q, K.shape[2], D, int(bool(causal)),
                                ctypes.c_void_p(st)), "attn_prefill")
+
+
+def attn_prefill_paged(Q, k_cache, v_cache, O, cu_seqlens_q, seq_lens_kv, block_tables,
+                       max_seqlen_q: int, causal: bool = True, stream=None) -> None:
+    """Prefill of packed query chunks (Q, O [total_q, H_q, D]; cu_seqlens_q [B+1])
+    against a paged cache holding seq_lens_kv[b] keys per sequence (its last
+    L_q keys are the chunk's own): query i sits at position L_kv - L_q + i."""
+    if Q.dim() != 3 or O.shape != Q.shape or k_cache.dim() != 4 or v_cache.shape != k_cache.shape:
+        raise ValueError("expected Q,O [total_q,H_q,D] and caches [num_blocks,H_kv,block_size,D]")
+    total_q, H_q, D = Q.shape
+    B = seq_lens_kv.shape[0]
+    if cu_seqlens_q.shape != (B + 1,) or block_tables.dim() != 2 or block_tables.shape[0] != B:
+        raise ValueError("expected cu_seqlens_q [B+1], seq_lens_kv [B], block_tables [B, max_blocks]")
+    ptrs = [_dev(Q, "Q", torch.float16), _dev(k_cache, "k_cache", torch.float16),
+            _dev(v_cache, "v_cache", torch.float16), _dev(O, "O", torch.float16),
+            _dev(cu_seqlens_q, "cu_seqlens_q", torch.int32), _dev(seq_lens_kv, "seq_lens_kv", torch.int32),
+            _dev(block_tables, "block_tables", torch.int32)]
+    st = _stream(stream, Q.device)
+    _check(load().attn_prefill_paged(*ptrs, B, int(max_seqlen_q), total_q, H_q, k_cache.shape[1], D,
+                                     block_tables.shape[1], k_cache.shape[2], k_cache.shape[0],
+                                     int(bool(causal)), ctypes.c_void_p(st)), "attn_prefill_paged")
 
 
 def attn_debug_prefill_stall(Q, K, V, O, stall_tile: int, causal: bool = True, stream=None) -> None:

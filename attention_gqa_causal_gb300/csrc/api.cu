@@ -129,6 +129,36 @@ ATTN_API int attn_prefill(const void* Q, const void* K, const void* V, void* O, 
     return prefill_checked(Q, K, V, O, B, S, H_q, H_kv, D, causal, -1, stream);
 }
 
+ATTN_API int attn_prefill_paged(const void* Q, const void* k_cache, const void* v_cache, void* O,
+                                const int* cu_seqlens_q, const int* seq_lens_kv,
+                                const int* block_tables, int B, int max_seqlen_q, int total_q,
+                                int H_q, int H_kv, int D, int max_blocks_per_seq, int block_size,
+                                long long num_blocks, int causal, cudaStream_t stream)
+{
+    if (B < 0 || max_seqlen_q < 0 || total_q < 0 || max_blocks_per_seq < 1 || num_blocks < 0 ||
+        check_heads(H_q, H_kv) != ATTN_OK)
+        return ATTN_ERR_INVALID_ARG;
+    if (D != attn::kHeadDim || block_size != attn::kPageSize)
+        return ATTN_ERR_UNSUPPORTED;
+    if (B == 0 || total_q == 0 || max_seqlen_q == 0)
+        return ATTN_OK;
+    if (num_blocks < 1 || !Q || !k_cache || !v_cache || !O || !cu_seqlens_q || !seq_lens_kv ||
+        !block_tables)
+        return ATTN_ERR_INVALID_ARG;
+    if (!aligned(Q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(O, 16) ||
+        !aligned(cu_seqlens_q, 4) || !aligned(seq_lens_kv, 4) || !aligned(block_tables, 4))
+        return ATTN_ERR_INVALID_ARG;
+    const size_t qbytes = (size_t)total_q * H_q * D * 2;
+    const size_t cache_bytes = (size_t)num_blocks * H_kv * block_size * D * 2;
+    if (overlap(O, qbytes, Q, qbytes) || overlap(O, qbytes, k_cache, cache_bytes) ||
+        overlap(O, qbytes, v_cache, cache_bytes))
+        return ATTN_ERR_INVALID_ARG;
+    const cudaError_t e = attn::launch_prefill_paged(
+        Q, k_cache, v_cache, O, cu_seqlens_q, seq_lens_kv, block_tables, B, max_seqlen_q, total_q,
+        H_q, H_kv, max_blocks_per_seq, num_blocks, causal, stream);
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
 ATTN_API int attn_debug_prefill_stall(const void* Q, const void* K, const void* V, void* O, int B,
                                       int S, int H_q, int H_kv, int D, int causal, int stall_tile,
                                       cudaStream_t stream)

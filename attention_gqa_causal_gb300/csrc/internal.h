@@ -18,6 +18,7 @@ enum DeviceError : int {
     kDevErrTmemAlloc = 8,      // TMEM base address outside the expected range
     kDevErrSmemLayout = 16,    // dynamic shared memory base too misaligned for the tile layout
     kDevErrBadSlot = 32,       // a slot_mapping entry outside [-1, num_blocks * block_size)
+    kDevErrBadLengths = 64,    // paged prefill: a chunk longer than its context (L_q > L_kv)
 };
 
 // Set by the kernels (atomicOr); defined in decode.cu.  Device address of the
@@ -64,5 +65,15 @@ int record_cuda_error(cudaError_t e);
 // load in every CTA, so the waits on it run out and report a timeout.
 cudaError_t launch_prefill(const void* Q, const void* K, const void* V, void* O, int B, int S,
                            int H_q, int H_kv, int causal, int stall_tile, cudaStream_t stream);
+
+// Prefill of packed query chunks ([total_q, H_q, 128], cu_seqlens_q [B+1])
+// against a paged cache ([num_blocks, H_kv, 16, 128]) holding seq_lens_kv[b]
+// keys per sequence; query i of sequence b sits at position
+// seq_lens_kv[b] - L_q(b) + i.
+cudaError_t launch_prefill_paged(const void* Q, const void* k_cache, const void* v_cache, void* O,
+                                 const int* cu_seqlens_q, const int* seq_lens_kv,
+                                 const int* block_tables, int B, int max_seqlen_q, int total_q,
+                                 int H_q, int H_kv, int max_blocks_per_seq, long long num_blocks,
+                                 int causal, cudaStream_t stream);
 
 }  // namespace attn

@@ -1,5 +1,6 @@
 // prefill.cu -- causal / full grouped-query attention prefill on sm_103a
-// tensor cores (tcgen05 + TMEM + TMA).
+// tensor cores (tcgen05 + TMEM + TMA), over contiguous K/V or over a paged
+// KV cache with packed variable-length query chunks.
 //
 // Operation ("Tutorial: Adding a New Kernel to RL.cu", add-cuda-kernel page,
 // include/kernels/attention.cuh, "Flash Attention 2 -- Prefill"): Q,O are
@@ -10,11 +11,15 @@
 // one the same page's kernel walks per key and the "GRPO-CUDA Project Memory"
 // page summarises under "Attention kernel design"; here it runs per 128-key
 // tile on tensor-core scores.
+// The paged form takes K/V from the cache layout of the same header's "Paged
+// Attention -- Decode" ([num_blocks, H_kv, 16, D] through block_tables) and
+// packed query chunks whose first query sits after a cached prefix
+// (L_kv - L_q keys): query i of a sequence attends to keys <= L_kv - L_q + i.
 //
 // GB300 design (one CTA per SM, 320 threads):
 //   warps 0-3  softmax of Q tile 0 (TMEM lanes 0..127 = its rows)
 //   warps 4-7  softmax of Q tile 1
-//   warp  8    MMA issuer (one lane) + TMEM allocation
+//   warp  8    MMA warp (one lane issues) + TMEM allocation
 //   warp  9    TMA producer (one lane)
 // A CTA owns two 128-row Q tiles that read the same K/V: two query heads of
 // one GQA group over the same rows when the group size is even (identical
@@ -35,9 +40,9 @@
 // "S ready" to "P ready" that the tensor core waits for.
 // TMEM: S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512) columns.
 // SMEM: Q0,Q1 (32 KB each), 2 K stages, 3 V stages (32 KB each), all
-// 128-byte swizzled as written by TMA boxes of 64 x 128.  Key tiles wholly
-// above the diagonal are never loaded or multiplied; only the diagonal tile
-// is masked.
+// 128-byte swizzled as written by TMA boxes of 64 x 128 (contiguous K/V) or
+// 64 x 16 (one cache page).  Key tiles wholly above the diagonal are never
+// loaded or multiplied; only the diagonal tile is masked.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -56,6 +61,7 @@ namespace {
 constexpr int BM = 128;  // query rows per tile
 constexpr int BN = 128;  // keys per tile
 constexpr int D = kHeadDim;
+constexpr int kPagesPerTile = BN / kPageSize;
 constexpr int kMmaWarp = 8;
 constexpr int kTmaWarp = 9;
 constexpr int kThreads = 10 * 32;
@@ -63,6 +69,7 @@ constexpr int kKStages = 2;
 constexpr int kVStages = 3;
 constexpr uint32_t kTileBytes = BM * D * 2;      // 32 KB
 constexpr uint32_t kBoxBytes = kTileBytes / 2;   // 16 KB: 128 rows x 64 halves
+constexpr uint32_t kPageBoxBytes = kPageSize * 64 * 2;  // 2 KB: 16 rows x 64 halves
 constexpr uint32_t kSmemQ = 0;
 constexpr uint32_t kSmemK = 2 * kTileBytes;
 constexpr uint32_t kSmemV = kSmemK + kKStages * kTileBytes;
@@ -74,20 +81,31 @@ constexpr float kLog2e = 1.4426950408889634f;
 struct PrefillArgs {
     __half* O;
     int* err;
-    int B, S, H_q, H_kv;
+    int B, S, H_q, H_kv;   // B: batch (contiguous) or number of sequences (paged); S unused when paged
     int group;          // H_q / H_kv
     int head_pairs;     // 1: the two tiles are two heads; 0: two row tiles of one head
     int units_per_mb;   // B * H_kv * (tile pairs per kv head)
-    int n_mb;           // number of row blocks
+    int n_mb;           // number of row blocks (of the longest chunk when paged)
     int causal;
     float scale_log2;   // log2(e) / sqrt(D)
     int stall_tile;     // failure-detection test only: key tile whose K load is withheld (-1: none)
+    // paged form only
+    const int* cu_q;          // [B+1] query chunk offsets into packed Q / O
+    const int* seq_lens_kv;   // [B] context lengths (prefix + chunk)
+    const int* block_tables;  // [B, max_blocks]
+    int max_blocks;
 };
 
 struct Unit {
     int b, g, head[2], row0[2], n_kv;
+    int q_base;  // first packed row of the sequence (paged) or b*S (contiguous)
+    int Lq, Lkv, off;  // chunk length, context length, off = Lkv - Lq (position of query 0)
+    int n_pages;
+    int flags;   // device error bits found while decoding the unit
+    bool valid;
 };
 
+template <bool PAGED>
 __device__ __forceinline__ Unit decode_unit(const PrefillArgs& a, int u)
 {
     Unit w;
@@ -108,8 +126,34 @@ __device__ __forceinline__ Unit decode_unit(const PrefillArgs& a, int u)
         w.row0[0] = mb * 2 * BM;
         w.row0[1] = w.row0[0] + BM;
     }
-    const int last_row = min(a.S - 1, w.row0[1] + BM - 1);
-    w.n_kv = a.causal ? last_row / BN + 1 : (a.S + BN - 1) / BN;
+    w.flags = 0;
+    w.valid = true;
+    if (!PAGED) {
+        w.q_base = w.b * a.S;
+        w.Lq = w.Lkv = a.S;
+    } else {
+        w.q_base = a.cu_q[w.b];
+        w.Lq = a.cu_q[w.b + 1] - w.q_base;
+        w.Lkv = a.seq_lens_kv[w.b];
+        const int max_len = a.max_blocks * kPageSize;
+        if (w.Lkv > max_len) {
+            w.flags |= kDevErrSeqTooLong;
+            w.Lkv = max_len;
+        }
+        if (w.Lq < 0 || w.Lq > w.Lkv) {
+            w.flags |= kDevErrBadLengths;
+            w.valid = false;
+        }
+        if (w.Lq > a.n_mb * (a.head_pairs ? BM : 2 * BM))
+            w.flags |= kDevErrBadLengths;  // longer than max_seqlen_q: its tail rows are not computed
+        if (w.row0[0] >= w.Lq)
+            w.valid = false;  // this row block is past the end of the chunk
+    }
+    w.off = w.Lkv - w.Lq;
+    w.n_pages = (w.Lkv + kPageSize - 1) / kPageSize;
+    const int last_row = min(w.Lq - 1, w.row0[1] + BM - 1);
+    const int all_tiles = (w.Lkv + BN - 1) / BN;
+    w.n_kv = a.causal ? min((w.off + last_row) / BN + 1, all_tiles) : all_tiles;
     return w;
 }
 
@@ -166,6 +210,7 @@ __device__ __forceinline__ void exp_pack32(uint32_t (&r)[32], float c, float neg
     }
 }
 
+template <bool PAGED>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const PrefillArgs a)
@@ -179,10 +224,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             atomicOr(a.err, kDevErrSmemLayout);
         return;
     }
-    SmemCtl& ctl = *reinterpret_cast<SmemCtl*>(smem_raw + (sbase - raw) + kSmemBytes);
+    uint8_t* const smem = smem_raw + (sbase - raw);  // generic pointer to the aligned base
+    SmemCtl& ctl = *reinterpret_cast<SmemCtl*>(smem + kSmemBytes);
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    const Unit w = decode_unit(a, blockIdx.x);
+    const Unit w = decode_unit<PAGED>(a, blockIdx.x);
+    if (w.flags && threadIdx.x == 0)
+        atomicOr(a.err, w.flags);
+    if (!w.valid)
+        return;  // uniform over the CTA, before any barrier or allocation
     volatile int* abort = &ctl.abort;
 
     if (threadIdx.x == 0) {
@@ -222,9 +272,35 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             const uint32_t qbar = smem_u32(&ctl.q_full);
             mbar_arrive_expect_tx(qbar, 2 * kTileBytes);
             for (int t = 0; t < 2; ++t)
-                for (int h = 0; h < 2; ++h)
-                    tma_load_4d(sbase + kSmemQ + t * kTileBytes + h * kBoxBytes, &tmQ, qbar, h * 64,
-                                w.head[t], w.row0[t], w.b);
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t dst = sbase + kSmemQ + t * kTileBytes + h * kBoxBytes;
+                    if (PAGED)
+                        tma_load_3d(dst, &tmQ, qbar, h * 64, w.head[t], w.q_base + w.row0[t]);
+                    else
+                        tma_load_4d(dst, &tmQ, qbar, h * 64, w.head[t], w.row0[t], w.b);
+                }
+            const int* trow = PAGED ? a.block_tables + (size_t)w.b * a.max_blocks : nullptr;
+            // one K or V tile into `dst`: a 64 x 128 box per half (contiguous), or
+            // one 64 x 16 box per half and page (paged; a page past the context, or
+            // any id outside the cache, reads as zeros)
+            auto load_tile = [&](const CUtensorMap* map, uint32_t dst, uint32_t bar, int j) {
+                if (PAGED) {
+                    int phys[kPagesPerTile];
+#pragma unroll
+                    for (int k = 0; k < kPagesPerTile; ++k) {
+                        const int p = j * kPagesPerTile + k;
+                        phys[k] = p < w.n_pages ? trow[p] : -1;
+                    }
+#pragma unroll
+                    for (int k = 0; k < kPagesPerTile; ++k)
+                        for (int h = 0; h < 2; ++h)
+                            tma_load_4d(dst + h * kBoxBytes + k * kPageBoxBytes, map, bar, h * 64, 0,
+                                        w.g, phys[k]);
+                } else {
+                    for (int h = 0; h < 2; ++h)
+                        tma_load_4d(dst + h * kBoxBytes, map, bar, h * 64, w.g, j * BN, w.b);
+                }
+            };
             int n_k = 0, n_v = 0;  // K / V tiles issued so far
             bool ok = true;
             for (int j = 0; j < w.n_kv && ok; ++j) {
@@ -235,9 +311,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 const uint32_t kbar = smem_u32(&ctl.k_full[sk]);
                 if (j != a.stall_tile) {
                     mbar_arrive_expect_tx(kbar, kTileBytes);
-                    for (int h = 0; h < 2; ++h)
-                        tma_load_4d(sbase + kSmemK + sk * kTileBytes + h * kBoxBytes, &tmK, kbar,
-                                    h * 64, w.g, j * BN, w.b);
+                    load_tile(&tmK, sbase + kSmemK + sk * kTileBytes, kbar, j);
                 }
                 ++n_k;
                 const int sv = j % kVStages;
@@ -246,9 +320,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     break;
                 const uint32_t vbar = smem_u32(&ctl.v_full[sv]);
                 mbar_arrive_expect_tx(vbar, kTileBytes);
-                for (int h = 0; h < 2; ++h)
-                    tma_load_4d(sbase + kSmemV + sv * kTileBytes + h * kBoxBytes, &tmV, vbar,
-                                h * 64, w.g, j * BN, w.b);
+                load_tile(&tmV, sbase + kSmemV + sv * kTileBytes, vbar, j);
                 ++n_v;
             }
             if (!ok)
@@ -272,68 +344,97 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             }
         }
     } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc_s = idesc_f16_f32(BM, BN, false, false);
-            const uint32_t idesc_o = idesc_f16_f32(BM, D, false, true);
-            // descriptors of the first tile of each region; moving within a region
-            // only adds (byte offset >> 4) to the start-address field (all shared
-            // addresses are below 256 KB, so the 14-bit field cannot overflow)
-            const uint64_t dq = sdesc_sw128(sbase + kSmemQ, 16, 1024);
-            const uint64_t dk = sdesc_sw128(sbase + kSmemK, 16, 1024);
-            const uint64_t dv = sdesc_sw128(sbase + kSmemV, kBoxBytes, 1024);
-            auto issue_s = [&](int t, int s) {
-                const uint64_t aq = dq + ((t * kTileBytes) >> 4);
-                const uint64_t bk = dk + ((s * kTileBytes) >> 4);
+        // ------------------------------------------------------------ MMA warp
+        // The whole warp follows the schedule (so it can clear shared memory
+        // when needed); lane 0 issues the MMAs and commits.
+        const bool leader = lane == 0;
+        const uint32_t idesc_s = idesc_f16_f32(BM, BN, false, false);
+        const uint32_t idesc_o = idesc_f16_f32(BM, D, false, true);
+        // descriptors of the first tile of each region; moving within a region
+        // only adds (byte offset >> 4) to the start-address field (all shared
+        // addresses are below 256 KB, so the 14-bit field cannot overflow)
+        const uint64_t dq = sdesc_sw128(sbase + kSmemQ, 16, 1024);
+        const uint64_t dk = sdesc_sw128(sbase + kSmemK, 16, 1024);
+        const uint64_t dv = sdesc_sw128(sbase + kSmemV, kBoxBytes, 1024);
+        auto issue_s = [&](int t, int s) {
+            const uint64_t aq = dq + ((t * kTileBytes) >> 4);
+            const uint64_t bk = dk + ((s * kTileBytes) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = ((kk / 4) * kBoxBytes + (kk % 4) * 32) >> 4;
-                    mma_f16_ss(tmem + t * BN, aq + off, bk + off, idesc_s, kk > 0);
-                }
-            };
-            auto issue_o = [&](int t, int s, bool acc) {
-                const uint64_t bv = dv + ((s * kTileBytes) >> 4);
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = ((kk / 4) * kBoxBytes + (kk % 4) * 32) >> 4;
+                mma_f16_ss(tmem + t * BN, aq + off, bk + off, idesc_s, kk > 0);
+            }
+        };
+        auto issue_o = [&](int t, int s, bool acc) {
+            const uint64_t bv = dv + ((s * kTileBytes) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_f16_ts(tmem + 256 + t * D, tmem + t * BN + kk * 8, bv + ((kk * 2048) >> 4),
-                               idesc_o, (acc || kk > 0) ? 1u : 0u);
-            };
-            bool ok = mbar_wait(smem_u32(&ctl.q_full), 0, abort) &&
-                      mbar_wait(smem_u32(&ctl.k_full[0]), 0, abort);
-            if (ok) {
-                tc_fence_after();
+            for (int kk = 0; kk < BN / 16; ++kk)
+                mma_f16_ts(tmem + 256 + t * D, tmem + t * BN + kk * 8, bv + ((kk * 2048) >> 4),
+                           idesc_o, (acc || kk > 0) ? 1u : 0u);
+        };
+        auto wait = [&](uint64_t& bar, uint32_t parity) {
+            return __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar), parity, abort));
+        };
+        bool ok = wait(ctl.q_full, 0) && wait(ctl.k_full[0], 0);
+        if (ok) {
+            tc_fence_after();
+            if (leader) {
                 issue_s(0, 0);
                 mma_commit(smem_u32(&ctl.s_full[0]));
                 issue_s(1, 0);
                 mma_commit(smem_u32(&ctl.s_full[1]));
                 mma_commit(smem_u32(&ctl.k_empty[0]));
             }
-            for (int j = 0; j < w.n_kv && ok; ++j) {
-                const int sv = j % kVStages;
-                const uint32_t phv = (j / kVStages) & 1;
-                const int sk1 = (j + 1) % kKStages;
-                const uint32_t phk1 = ((j + 1) / kKStages) & 1;
-                const bool more = j + 1 < w.n_kv;
-                ok = mbar_wait(smem_u32(&ctl.p_full[0]), j & 1, abort) &&
-                     mbar_wait(smem_u32(&ctl.v_full[sv]), phv, abort);
-                if (!ok)
-                    break;
-                tc_fence_after();
+            __syncwarp();
+        }
+        for (int j = 0; j < w.n_kv && ok; ++j) {
+            const int sv = j % kVStages;
+            const uint32_t phv = (j / kVStages) & 1;
+            const int sk1 = (j + 1) % kKStages;
+            const uint32_t phk1 = ((j + 1) / kKStages) & 1;
+            const bool more = j + 1 < w.n_kv;
+            ok = wait(ctl.p_full[0], j & 1) && wait(ctl.v_full[sv], phv);
+            if (!ok)
+                break;
+            if (PAGED && (j + 1) * BN > w.Lkv) {
+                // Keys from L_kv to the end of the last page are cache slots that may
+                // hold anything (even NaN, and 0 * NaN would reach O through the MMA
+                // although their P is 0): zero those V rows.  Later pages arrive
+                // from TMA as zeros already.
+                const int r0 = w.Lkv - j * BN;
+                const int r1 = min(BN, w.n_pages * kPageSize - j * BN);
+                uint8_t* vt = smem + kSmemV + sv * kTileBytes;
+                for (int idx = lane; idx < (r1 - r0) * 16; idx += 32) {
+                    const int rr = r0 + idx / 16, hh = (idx % 16) / 8, c16 = idx % 8;
+                    *reinterpret_cast<uint4*>(vt + hh * kBoxBytes + rr * 128 + c16 * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            tc_fence_after();
+            if (leader) {
                 issue_o(0, sv, j > 0);
                 if (!more)
                     mma_commit(smem_u32(&ctl.o_full[0]));
-                if (more) {
-                    ok = mbar_wait(smem_u32(&ctl.k_full[sk1]), phk1, abort);
-                    if (!ok)
-                        break;
-                    tc_fence_after();
-                    issue_s(0, sk1);
-                    mma_commit(smem_u32(&ctl.s_full[0]));
-                }
-                ok = mbar_wait(smem_u32(&ctl.p_full[1]), j & 1, abort);
+            }
+            __syncwarp();
+            if (more) {
+                ok = wait(ctl.k_full[sk1], phk1);
                 if (!ok)
                     break;
                 tc_fence_after();
+                if (leader) {
+                    issue_s(0, sk1);
+                    mma_commit(smem_u32(&ctl.s_full[0]));
+                }
+                __syncwarp();
+            }
+            ok = wait(ctl.p_full[1], j & 1);
+            if (!ok)
+                break;
+            tc_fence_after();
+            if (leader) {
                 issue_o(1, sv, j > 0);
                 mma_commit(smem_u32(&ctl.v_empty[sv]));
                 if (!more)
@@ -344,6 +445,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     mma_commit(smem_u32(&ctl.k_empty[sk1]));
                 }
             }
+            __syncwarp();
+        }
+        if (leader) {
             if (!ok)
                 flag_abort(&ctl, a.err);
             // drain: all MMAs issued by this thread are complete before TMEM is released
@@ -358,11 +462,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         const int row = quad * 32 + lane;   // row within the tile = TMEM lane
         const int my_row0 = t ? w.row0[1] : w.row0[0];
         const int my_head = t ? w.head[1] : w.head[0];
-        const int q_row = my_row0 + row;    // row within the sequence
+        const int q_row = my_row0 + row;    // query row within the sequence (chunk)
         const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t tS = tmem + lane_addr + t * BN;
         const uint32_t tO = tmem + lane_addr + 256 + t * D;
         const float c = a.scale_log2;
+        // keys [0, key_end) are visible to this row: up to its own position
+        // (off + q_row) with the causal mask, else the whole context
+        const int key_end = a.causal ? min(w.off + q_row + 1, w.Lkv) : w.Lkv;
         float m_ref = -CUDART_INF_F;  // reference max (log2 units) shared by l and O
         float l_sum = 0.f;
         bool ok = true;
@@ -371,8 +478,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             if (!ok)
                 break;
             tc_fence_after();
-            const int kv0 = j * BN;
-            const int limit = a.causal ? min(q_row + 1, a.S) - kv0 : a.S - kv0;
+            const int limit = key_end - j * BN;
             const bool masked = __any_sync(0xffffffffu, limit < BN);
             uint32_t sr[4][32];
             float rs[8];
@@ -459,8 +565,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         } else {
             tc_fence_after();
             const float inv = 1.f / l_sum;
-            const bool store = q_row < a.S;
-            __half* dst = a.O + (((size_t)w.b * a.S + q_row) * a.H_q + my_head) * D;
+            const bool store = q_row < w.Lq;
+            __half* dst = a.O + ((size_t)(w.q_base + q_row) * a.H_q + my_head) * D;
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
                 uint32_t orr[32];
@@ -512,21 +618,87 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// [B,S,H,128] FP16 tensor, boxes of 64 head-dim x 1 head x 128 rows x 1 batch, 128B swizzle.
-bool make_bshd_map(CUtensorMap* m, const void* ptr, int B, int S, int H)
+// FP16 tensor map, 128-byte swizzle, zero fill out of bounds.  dims/strides
+// innermost first (strides in bytes, for dims 1..rank-1).
+bool make_map(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
+              const cuuint64_t* strides, const cuuint32_t* box)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc)
         return false;
+    const cuuint32_t es[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, rank, const_cast<void*>(ptr), dims, strides, box,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+// [B,S,H,128]: boxes of 64 head-dim x 1 head x 128 rows x 1 batch.
+bool make_bshd_map(CUtensorMap* m, const void* ptr, int B, int S, int H)
+{
     const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
     const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2,
                                    (cuuint64_t)S * H * D * 2};
     const cuuint32_t box[4] = {64, 1, BM, 1};
-    const cuuint32_t es[4] = {1, 1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(ptr), dims, strides, box,
-               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-           CUDA_SUCCESS;
+    return make_map(m, ptr, 4, dims, strides, box);
+}
+
+// packed [total, H, 128]: boxes of 64 head-dim x 1 head x 128 rows.
+bool make_packed_map(CUtensorMap* m, const void* ptr, int total, int H)
+{
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)total};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+    const cuuint32_t box[3] = {64, 1, BM};
+    return make_map(m, ptr, 3, dims, strides, box);
+}
+
+// paged cache [num_blocks, H_kv, 16, 128]: boxes of 64 head-dim x 16 slots (one page).
+bool make_cache_map(CUtensorMap* m, const void* ptr, long long num_blocks, int H_kv)
+{
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)kPageSize, (cuuint64_t)H_kv,
+                                (cuuint64_t)num_blocks};
+    const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)kPageSize * D * 2,
+                                   (cuuint64_t)H_kv * kPageSize * D * 2};
+    const cuuint32_t box[4] = {64, kPageSize, 1, 1};
+    return make_map(m, ptr, 4, dims, strides, box);
+}
+
+// the shared-memory opt-in is a per-device, per-kernel attribute
+template <bool PAGED>
+cudaError_t ensure_smem_attr()
+{
+    static std::mutex mtx;
+    static bool done[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= 64)
+        return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mtx);
+    if (!done[dev]) {
+        e = cudaFuncSetAttribute(prefill_kernel<PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSmemAlloc);
+        if (e != cudaSuccess)
+            return e;
+        done[dev] = true;
+    }
+    return cudaSuccess;
+}
+
+void fill_common(PrefillArgs& a, int B, int H_q, int H_kv, int rows, int causal)
+{
+    a.B = B;
+    a.H_q = H_q;
+    a.H_kv = H_kv;
+    a.group = H_q / H_kv;
+    a.head_pairs = (a.group % 2 == 0) ? 1 : 0;
+    const int pairs_per_g = a.head_pairs ? a.group / 2 : a.group;
+    a.n_mb = a.head_pairs ? (rows + BM - 1) / BM : (rows + 2 * BM - 1) / (2 * BM);
+    a.units_per_mb = B * H_kv * pairs_per_g;
+    a.causal = causal ? 1 : 0;
+    a.scale_log2 = kLog2e / sqrtf((float)D);
+    a.stall_tile = -1;
 }
 
 }  // namespace
@@ -534,25 +706,9 @@ bool make_bshd_map(CUtensorMap* m, const void* ptr, int B, int S, int H)
 cudaError_t launch_prefill(const void* Q, const void* K, const void* V, void* O, int B, int S,
                            int H_q, int H_kv, int causal, int stall_tile, cudaStream_t stream)
 {
-    // the shared-memory opt-in is a per-device attribute
-    static std::mutex attr_mutex;
-    static bool attr_done[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    cudaError_t e = ensure_smem_attr<false>();
     if (e != cudaSuccess)
         return e;
-    if (dev < 0 || dev >= 64)
-        return cudaErrorInvalidDevice;
-    {
-        std::lock_guard<std::mutex> lock(attr_mutex);
-        if (!attr_done[dev]) {
-            e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)kSmemAlloc);
-            if (e != cudaSuccess)
-                return e;
-            attr_done[dev] = true;
-        }
-    }
     CUtensorMap mq, mk, mv;
     if (!make_bshd_map(&mq, Q, B, S, H_q) || !make_bshd_map(&mk, K, B, S, H_kv) ||
         !make_bshd_map(&mv, V, B, S, H_kv))
@@ -562,22 +718,44 @@ cudaError_t launch_prefill(const void* Q, const void* K, const void* V, void* O,
     a.err = device_error_word();
     if (!a.err)
         return cudaErrorInvalidSymbol;
-    a.B = B;
+    fill_common(a, B, H_q, H_kv, S, causal);
     a.S = S;
-    a.H_q = H_q;
-    a.H_kv = H_kv;
-    a.group = H_q / H_kv;
-    a.head_pairs = (a.group % 2 == 0) ? 1 : 0;
-    const int pairs_per_g = a.head_pairs ? a.group / 2 : a.group;
-    a.n_mb = a.head_pairs ? (S + BM - 1) / BM : (S + 2 * BM - 1) / (2 * BM);
-    a.units_per_mb = B * H_kv * pairs_per_g;
-    a.causal = causal ? 1 : 0;
-    a.scale_log2 = kLog2e / sqrtf((float)D);
     a.stall_tile = stall_tile;
     const long long grid = (long long)a.units_per_mb * a.n_mb;
     if (grid > 0x7fffffffLL)
         return cudaErrorInvalidConfiguration;
-    prefill_kernel<<<(unsigned)grid, kThreads, kSmemAlloc, stream>>>(mq, mk, mv, a);
+    prefill_kernel<false><<<(unsigned)grid, kThreads, kSmemAlloc, stream>>>(mq, mk, mv, a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_paged(const void* Q, const void* k_cache, const void* v_cache, void* O,
+                                 const int* cu_seqlens_q, const int* seq_lens_kv,
+                                 const int* block_tables, int B, int max_seqlen_q, int total_q,
+                                 int H_q, int H_kv, int max_blocks_per_seq, long long num_blocks,
+                                 int causal, cudaStream_t stream)
+{
+    cudaError_t e = ensure_smem_attr<true>();
+    if (e != cudaSuccess)
+        return e;
+    CUtensorMap mq, mk, mv;
+    if (!make_packed_map(&mq, Q, total_q, H_q) || !make_cache_map(&mk, k_cache, num_blocks, H_kv) ||
+        !make_cache_map(&mv, v_cache, num_blocks, H_kv))
+        return cudaErrorInvalidValue;
+    PrefillArgs a{};
+    a.O = static_cast<__half*>(O);
+    a.err = device_error_word();
+    if (!a.err)
+        return cudaErrorInvalidSymbol;
+    fill_common(a, B, H_q, H_kv, max_seqlen_q, causal);
+    a.S = 0;
+    a.cu_q = cu_seqlens_q;
+    a.seq_lens_kv = seq_lens_kv;
+    a.block_tables = block_tables;
+    a.max_blocks = max_blocks_per_seq;
+    const long long grid = (long long)a.units_per_mb * a.n_mb;
+    if (grid > 0x7fffffffLL)
+        return cudaErrorInvalidConfiguration;
+    prefill_kernel<true><<<(unsigned)grid, kThreads, kSmemAlloc, stream>>>(mq, mk, mv, a);
     return cudaGetLastError();
 }
 

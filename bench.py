@@ -5,6 +5,8 @@ One step is one pass over every hot-path kernel on its workload:
   * causal GQA prefill   B=2, S=8192, H_q=32, H_kv=8, D=128   (headline: TFLOP/s,
     causal FLOPs counted as 2*B*H_q*S^2*D)
   * the same shape without the mask (the unmasked tensor-core ceiling)
+  * chunked prefill from the paged cache: 4 sequences, 6144 cached + 2048 new
+    tokens each, H 32/8 (FLOPs over each query's visible keys)
   * paged decode          256 sequences, lengths uniform on [128, 2048], H 16/8
   * paged decode          8 sequences x 32768 tokens, H 16/8
   * the 256-sequence decode step together with its KV append (two launches)
@@ -169,6 +171,21 @@ def build_legs(torch, ag, which):
             leg.config = {"B": cfg.B, "S": cfg.S, "H_q": cfg.H_q, "H_kv": cfg.H_kv, "D": cfg.D,
                           "causal": cfg.causal}
             legs.append(leg)
+    if which in ("all", "prefill_paged"):
+        cfg = W.CHUNKED_PREFILL
+        Qp, kc, vc, cu, skv, tables = W.chunked_prefill_inputs(cfg, seed=0)
+        t = [torch.from_numpy(x).cuda() for x in (Qp, kc, vc, cu, skv, tables)]
+        Op = torch.empty_like(t[0])
+        leg = Leg(cfg.name, "prefill", cfg.flops(), "TFLOP/s", 1)
+        leg.run = (lambda t=t, Op=Op, c=cfg: ag.attn_prefill_paged(
+            t[0], t[1], t[2], Op, t[3], t[4], t[5], c.chunk, causal=c.causal))
+        leg.host = {"Q": Qp, "k_cache": kc, "v_cache": vc, "cu_seqlens_q": cu, "seq_lens_kv": skv,
+                    "block_tables": tables}
+        leg.dev_in, leg.dev_out = tuple(t), Op
+        leg.config = {"num_seqs": cfg.num_seqs, "prefix": cfg.prefix, "chunk": cfg.chunk,
+                      "H_q": cfg.H_q, "H_kv": cfg.H_kv, "D": cfg.D, "causal": cfg.causal,
+                      "block_size": 16, "num_blocks": int(kc.shape[0])}
+        legs.append(leg)
     for cfg, key in ((W.DECODE_MIX, "decode"), (W.DECODE_LONG, "decode_long")):
         if which not in ("all", key) and not (key == "decode" and which == "decode_append"):
             continue
@@ -410,8 +427,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["all", "prefill", "prefill_full", "decode", "decode_long",
-                                           "decode_append"],
+    ap.add_argument("--workload", choices=["all", "prefill", "prefill_full", "prefill_paged", "decode",
+                                           "decode_long", "decode_append"],
                     default="all")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="CPU time budget of the oracle baseline sample")

@@ -59,6 +59,34 @@ ATTN_API int attn_prefill(const void* Q, const void* K, const void* V, void* O, 
                           int H_q, int H_kv, int D, int causal, cudaStream_t stream);
 
 /*
+ * Prefill of new query chunks against a paged KV cache (variable lengths,
+ * cached prefix): the chunked-prefill step that combines the prefill of
+ * "Flash Attention 2 -- Prefill" with the cache layout of "Paged Attention --
+ * Decode" (same header).  Sequence b contributes L_q = cu_seqlens_q[b+1] -
+ * cu_seqlens_q[b] queries, packed at rows cu_seqlens_q[b].. of Q and O; its
+ * context holds L_kv = seq_lens_kv[b] keys in the cache, the last L_q of them
+ * belonging to the chunk itself (its K/V appended already), so L_q <= L_kv.
+ * Query i sits at position L_kv - L_q + i; with causal != 0 it attends to
+ * keys 0..L_kv-L_q+i, else to all L_kv keys; scale 1/sqrt(D), g = h*H_kv/H_q.
+ * Q, O         : [total_q, H_q, D] FP16, total_q = cu_seqlens_q[B]
+ * k/v_cache    : [num_blocks, H_kv, block_size, D] FP16
+ * cu_seqlens_q : [B+1] int32 (0 first, non-decreasing); seq_lens_kv : [B] int32
+ * block_tables : [B, max_blocks_per_seq] int32
+ * max_seqlen_q : an upper bound of every L_q (sizes the launch).
+ * D must be 128 and block_size 16.  B, total_q or max_seqlen_q == 0 is a no-op.
+ * Cache slots past a context and table entries past its pages may hold
+ * anything; a page id outside [0, num_blocks) reads as zeros.  Device-checked
+ * preconditions (flagged, ATTN_ERR_BAD_INPUT): L_q <= L_kv (else the
+ * sequence is skipped), L_q <= max_seqlen_q (else its extra rows are not
+ * computed), L_kv <= max_blocks_per_seq*block_size (else clamped).
+ */
+ATTN_API int attn_prefill_paged(const void* Q, const void* k_cache, const void* v_cache, void* O,
+                                const int* cu_seqlens_q, const int* seq_lens_kv,
+                                const int* block_tables, int B, int max_seqlen_q, int total_q,
+                                int H_q, int H_kv, int D, int max_blocks_per_seq, int block_size,
+                                long long num_blocks, int causal, cudaStream_t stream);
+
+/*
  * Failure-detection test hook (not for production use): attn_prefill, except
  * that the K tile with index stall_tile (>= 0) is never loaded in any CTA
  * that reaches it.  The on-chip waits for that tile run out after their
@@ -203,7 +231,8 @@ ATTN_API int attn_release_workspace(void);
  * Read the device error word of the current device (synchronises the device).
  * *code receives the raw bits (1 timeout, 2 negative block id, 4 seq_len
  * beyond the table, 16 shared-memory layout did not fit, 32 slot out of
- * range); the return is ATTN_OK if it is 0, else ATTN_ERR_TIMEOUT
+ * range, 64 a paged-prefill chunk longer than its context or than
+ * max_seqlen_q); the return is ATTN_OK if it is 0, else ATTN_ERR_TIMEOUT
  * or ATTN_ERR_BAD_INPUT.  reset != 0 clears it.
  */
 ATTN_API int attn_get_device_error(int* code, int reset);

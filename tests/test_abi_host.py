@@ -141,3 +141,24 @@ def test_kv_append_validation():
     assert app(kn=0) == ag.ATTN_ERR_INVALID_ARG
     assert app(kc=A16) == ag.ATTN_ERR_INVALID_ARG                # cache overlaps the new rows
     assert app(T=0) == ag.ATTN_OK
+
+
+def test_prefill_paged_validation():
+    lib = ag.load()
+    LL = ctypes.c_longlong
+
+    def pp(Q=A16, kc=A16B, vc=A16B + 0x1000000, O=A16 + 0x100000, cu=A16 + 0x200000, sl=A16 + 0x200100,
+           bt=A16 + 0x200200, B=2, mq=64, tq=100, Hq=4, Hkv=2, D=128, mb=8, bs=16, nb=16, causal=1):
+        return lib.attn_prefill_paged(P(Q), P(kc), P(vc), P(O), P(cu), P(sl), P(bt), B, mq, tq, Hq, Hkv, D,
+                                      mb, bs, LL(nb), causal, P(0))
+
+    assert pp(D=64) == ag.ATTN_ERR_UNSUPPORTED
+    assert pp(bs=32) == ag.ATTN_ERR_UNSUPPORTED
+    assert pp(Hq=6, Hkv=4) == ag.ATTN_ERR_INVALID_ARG
+    assert pp(B=-1) == ag.ATTN_ERR_INVALID_ARG
+    assert pp(mb=0) == ag.ATTN_ERR_INVALID_ARG
+    assert pp(nb=0) == ag.ATTN_ERR_INVALID_ARG
+    assert pp(cu=0) == ag.ATTN_ERR_INVALID_ARG
+    assert pp(O=A16 + 64) == ag.ATTN_ERR_INVALID_ARG          # O overlaps Q
+    assert pp(O=A16B + 128) == ag.ATTN_ERR_INVALID_ARG        # O overlaps the K cache
+    assert pp(B=0) == ag.ATTN_OK and pp(tq=0) == ag.ATTN_OK and pp(mq=0) == ag.ATTN_OK

@@ -201,3 +201,39 @@ def decode_inputs(cfg: DecodeConfig, seed: int = 0, seq_lens=None) -> DecodeInpu
     k = normal_fp16(seed, 1, shape)
     v = normal_fp16(seed, 2, shape)
     return DecodeInputs(q, k, v, tables, seq_lens)
+
+
+@dataclass(frozen=True)
+class ChunkedPrefillConfig:
+    """New query chunks after a cached prefix, K/V in the paged cache."""
+    name: str
+    num_seqs: int
+    prefix: int
+    chunk: int
+    H_q: int
+    H_kv: int
+    D: int = 128
+    causal: bool = True
+
+    def flops(self) -> float:
+        """4*D*H_q per (query, visible key) pair: query i of a chunk sees
+        prefix + i + 1 keys (causal) or prefix + chunk keys."""
+        Lq, off = self.chunk, self.prefix
+        pairs = Lq * off + Lq * (Lq + 1) / 2 if self.causal else Lq * (off + Lq)
+        return 4.0 * self.D * self.H_q * self.num_seqs * pairs
+
+
+CHUNKED_PREFILL = ChunkedPrefillConfig("prefill_paged_n4_prefix6144_chunk2048_h32_kv8", 4, 6144,
+                                       2048, 32, 8)
+
+
+def chunked_prefill_inputs(cfg: ChunkedPrefillConfig, seed: int = 0):
+    """Packed Q [total_q, H_q, D] (stream 0), paged K/V caches (streams 1/2)
+    laid out by decode_layout, cu_seqlens_q and seq_lens_kv."""
+    lens_kv = np.full(cfg.num_seqs, cfg.prefix + cfg.chunk, np.int32)
+    tables, nb = decode_layout(lens_kv, 16, (cfg.prefix + cfg.chunk + 15) // 16, seed)
+    kc = normal_fp16(seed, 1, (nb, cfg.H_kv, 16, cfg.D))
+    vc = normal_fp16(seed, 2, (nb, cfg.H_kv, 16, cfg.D))
+    Q = normal_fp16(seed, 0, (cfg.num_seqs * cfg.chunk, cfg.H_q, cfg.D))
+    cu = np.arange(0, (cfg.num_seqs + 1) * cfg.chunk, cfg.chunk, dtype=np.int32)
+    return Q, kc, vc, cu, lens_kv, tables
