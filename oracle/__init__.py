@@ -228,3 +228,23 @@ def prefill_paged(Q, k_cache, v_cache, cu_seqlens_q, seq_lens_kv, block_tables, 
     lib.oracle_prefill_paged(_ptr(Q), _ptr(kc), _ptr(vc), _ptr(cu), _ptr(sl), _ptr(bt), B, H_q,
                              H_kv, D, bt.shape[1], bs, int(bool(causal)), _ptr(O), _ptr(lse))
     return (O, lse) if with_lse else O
+
+
+def qk_norm_rope(x, weight, positions, base, eps=1e-6):
+    """Per-head RMSNorm (skipped when ``weight`` is None) then NeoX rotary
+    embedding of x [T, H, D] at ``positions`` [T]; float64 result."""
+    x = _half(x)
+    T, H, D = x.shape
+    assert D % 2 == 0 and D <= 1024
+    w = None if weight is None else _half(weight)
+    assert w is None or w.shape == (D,)
+    pos = _i32(positions)
+    assert pos.shape == (T,)
+    out = np.empty((T, H, D), np.float64)
+    lib = _load()
+    p, i, d = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
+    lib.oracle_qk_norm_rope.argtypes = [p, p, p, i, i, i, d, d, p]
+    lib.oracle_qk_norm_rope.restype = None
+    lib.oracle_qk_norm_rope(_ptr(x), None if w is None else _ptr(w), _ptr(pos), T, H, D,
+                            float(base), float(eps), _ptr(out))
+    return out

@@ -35,10 +35,14 @@
  * Readings where the pages are silent (each also listed in the design notes):
  *  - an empty key set (seq_len == 0) gives o = 0 and lse = -inf;
  *  - causal=0 attends to all S keys;
- *  - NaN/Inf inputs propagate with no special handling.
+ *  - NaN/Inf inputs propagate with no special handling;
+ *  - RoPE pairs element i with element i + D/2 (the split-half form the
+ *    Qwen3 notes name) and pair i turns by pos * base^(-2i/D); the base is a
+ *    parameter (the pages print none).
  *
- * Every function here is pinned by tests against torch float64 SDPA on tiny
- * shapes, closed forms and invariants; see tests/test_oracle_pins.py.
+ * Every function here is pinned by tests against torch float64 SDPA and
+ * rms_norm on tiny shapes, a complex-number form of the rotation, closed forms
+ * and invariants; see tests/test_oracle_pins.py.
  */
 #include <math.h>
 #include <stdint.h>
@@ -422,5 +426,55 @@ void oracle_prefill_paged(const uint16_t *Q, const uint16_t *k_cache, const uint
                 lse[r] = l;
         }
         free(scores);
+    }
+}
+
+/*
+ * Per-head QK-norm followed by rotary position embedding: the prologue that
+ * turns projected q/k rows into the attention inputs.
+ *
+ *  - "GRPO-CUDA Project Memory" page, "Qwen3-Specific Notes": RMSNorm over
+ *    each head's D = 128 values, applied before RoPE, eps 1e-6; "Model forward
+ *    pass": QK-norm -> RoPE -> KV append -> attention.
+ *  - same page, "RoPE design": NeoX split-half pairing, element i rotates with
+ *    element i + D/2 for i < D/2; rotation arithmetic in full precision.
+ *  - Kimi-K2.6 KernelBench trace (fused cross-attention page): pair i turns by
+ *    the angle pos * base^(-2i/D).
+ *
+ *   r            = sqrt(mean_d x[d]^2 + eps)
+ *   y[d]         = w[d] * x[d] / r          (y = x when w is NULL: RoPE only)
+ *   a_i          = pos * base^(-2i/D),       i in [0, D/2)
+ *   out[i]       = y[i] cos a_i - y[i + D/2] sin a_i
+ *   out[i + D/2] = y[i + D/2] cos a_i + y[i] sin a_i
+ *
+ * x: [T, H, D] fp16 bits; w: [D] fp16 bits or NULL; positions: [T] int32, the
+ * absolute position of each token; out: [T, H, D] double.
+ */
+void oracle_qk_norm_rope(const uint16_t *x, const uint16_t *w, const int32_t *positions, int T,
+                         int H, int D, double base, double eps, double *out)
+{
+    const int half = D / 2;
+#pragma omp parallel for schedule(dynamic, 16)
+    for (long r = 0; r < (long)T * H; r++) {
+        const int t = (int)(r / H);
+        const uint16_t *xr = x + r * D;
+        double *o = out + r * D;
+        double y[1024];
+        double ss = 0.0;
+        for (int d = 0; d < D; d++) {
+            y[d] = oracle_half_to_double(xr[d]);
+            ss += y[d] * y[d];
+        }
+        if (w) {
+            const double rms = sqrt(ss / D + eps);
+            for (int d = 0; d < D; d++)
+                y[d] = oracle_half_to_double(w[d]) * y[d] / rms;
+        }
+        for (int i = 0; i < half; i++) {
+            const double a = (double)positions[t] * pow(base, -2.0 * i / D);
+            const double c = cos(a), s = sin(a);
+            o[i] = y[i] * c - y[i + half] * s;
+            o[i + half] = y[i + half] * c + y[i] * s;
+        }
     }
 }

@@ -24,6 +24,12 @@ MUTANTS = {
                        "c.g = (int)(h % H_kv);\n    attend_one(q + ((long)n * H_q + h) * D"),
     "paged_prefill_no_prefix_offset": ("const int n = causal ? Lkv - Lq + i + 1 : Lkv;",
                                        "const int n = causal ? i + 1 : Lkv;"),
+    "rope_sin_sign": ("o[i] = y[i] * c - y[i + half] * s;", "o[i] = y[i] * c + y[i + half] * s;"),
+    "rope_frequency_exponent": ("pow(base, -2.0 * i / D)", "pow(base, -1.0 * i / D)"),
+    "rope_position_by_row": ("const int t = (int)(r / H);", "const int t = (int)(r % T);"),
+    "norm_eps_dropped": ("sqrt(ss / D + eps)", "sqrt(ss / D)"),
+    "norm_mean_over_half": ("sqrt(ss / D + eps)", "sqrt(ss / half + eps)"),
+    "norm_weight_dropped": ("y[d] = oracle_half_to_double(w[d]) * y[d] / rms;", "y[d] = y[d] / rms;"),
 }
 
 PINS = [
@@ -36,6 +42,10 @@ PINS = [
     lambda: pins.test_lse_merge_of_segments_equals_whole([0, 1, 2, 33, 40]),
     pins.test_lse_merge_two_known_partials,
     pins.test_prefill_paged_equals_last_rows_of_full_causal_prefill,
+    lambda: pins.test_rope_frequencies_are_geometric_from_one(128),
+    pins.test_rope_equals_complex_rotation,
+    lambda: [pins.test_qk_norm_equals_torch_rms_norm_at_position_zero(s) for s in (1.0, 1e-4)],
+    pins.test_qk_norm_then_rope_order_and_weights,
 ]
 
 

@@ -376,3 +376,100 @@ def test_prefill_paged_noncausal_and_decode_special_case():
     for b in range(2):
         ref = _sdpa(Q[cu[b]:cu[b + 1]][None], K[b][None], V[b][None], causal=False)[0]
         np.testing.assert_allclose(out[cu[b]:cu[b + 1]], ref, atol=1e-12)
+
+
+# ------------------------------------------------ QK-norm + RoPE prologue
+
+ROPE_BASE = 1.0e6
+
+
+def _complex_turn(y, positions, freqs):
+    """Rotate each split-half pair (y_i, y_{i+D/2}) as the complex number
+    y_i + 1j*y_{i+D/2} multiplied by exp(1j*pos*freq_i)."""
+    h = y.shape[-1] // 2
+    z = (y[..., :h] + 1j * y[..., h:]) * np.exp(1j * np.multiply.outer(positions, freqs))[:, None, :]
+    return np.concatenate([z.real, z.imag], axis=-1)
+
+
+def _recovered_freqs(D, base):
+    # a unit vector in pair i (element i = 1, element i+D/2 = 0) at position 1
+    # turns by freq_i; read the angle back with atan2 (freq <= 1 < pi)
+    h = D // 2
+    x = np.zeros((h, 1, D), np.float16)
+    x[np.arange(h), 0, np.arange(h)] = 1.0
+    out = oracle.qk_norm_rope(x, None, np.ones(h, np.int32), base)
+    i = np.arange(h)
+    return np.arctan2(out[i, 0, i + h], out[i, 0, i])
+
+
+@pytest.mark.parametrize("D", [128, 16])
+def test_rope_frequencies_are_geometric_from_one(D):
+    f = _recovered_freqs(D, ROPE_BASE)
+    assert abs(f[0] - 1.0) < 1e-15                               # pair 0 turns one radian per position
+    np.testing.assert_allclose(f[1:] / f[:-1], ROPE_BASE ** (-2.0 / D), rtol=1e-12)
+    # extrapolating one pair past the end reaches 1/base
+    assert abs(f[-1] * ROPE_BASE ** (-2.0 / D) * ROPE_BASE - 1.0) < 1e-9
+
+
+def test_rope_equals_complex_rotation():
+    rng = np.random.default_rng(70)
+    T, H, D = 11, 3, 128
+    x = _rand16(rng, (T, H, D))
+    pos = rng.integers(0, 40000, T).astype(np.int32)
+    pos[0] = 0
+    out = oracle.qk_norm_rope(x, None, pos, ROPE_BASE)
+    freqs = _recovered_freqs(D, ROPE_BASE)
+    ref = _complex_turn(x.astype(np.float64), pos.astype(np.float64), freqs)
+    np.testing.assert_allclose(out, ref, atol=1e-9)
+    np.testing.assert_array_equal(out[0], x[0].astype(np.float64))     # position 0 is the identity
+    # every pair keeps its length
+    h = D // 2
+    np.testing.assert_allclose(out[..., :h] ** 2 + out[..., h:] ** 2,
+                               x[..., :h].astype(np.float64) ** 2 + x[..., h:].astype(np.float64) ** 2,
+                               rtol=1e-12, atol=1e-14)
+
+
+def test_rope_scores_depend_only_on_relative_position():
+    rng = np.random.default_rng(71)
+    D = 128
+    q, k = _rand16(rng, (1, 1, D)), _rand16(rng, (1, 1, D))
+
+    def score(m, n):
+        a = oracle.qk_norm_rope(q, None, np.array([m], np.int32), ROPE_BASE)
+        b = oracle.qk_norm_rope(k, None, np.array([n], np.int32), ROPE_BASE)
+        return float((a * b).sum())
+    s = score(37, 5)
+    for c in (1, 100, 9000):
+        assert abs(score(37 + c, 5 + c) - s) < 1e-9 * (1 + abs(s))
+    assert abs(score(5, 37) - s) > 1e-3                               # the sign of m - n matters
+
+
+@pytest.mark.parametrize("scale", [1.0, 30.0, 1e-4])
+def test_qk_norm_equals_torch_rms_norm_at_position_zero(scale):
+    rng = np.random.default_rng(72)
+    T, H, D = 7, 4, 128
+    x = _rand16(rng, (T, H, D), scale)
+    w = (1.0 + 0.5 * rng.standard_normal(D)).astype(np.float16)
+    out = oracle.qk_norm_rope(x, w, np.zeros(T, np.int32), ROPE_BASE, eps=1e-6)
+    ref = F.rms_norm(torch.from_numpy(x.astype(np.float64)), (D,),
+                     torch.from_numpy(w.astype(np.float64)), eps=1e-6).numpy()
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-14)
+
+
+def test_qk_norm_then_rope_order_and_weights():
+    # RMSNorm first, RoPE second: with non-uniform weights the two do not commute
+    rng = np.random.default_rng(73)
+    T, H, D = 9, 2, 128
+    x = _rand16(rng, (T, H, D))
+    w = rng.uniform(0.2, 3.0, D).astype(np.float16)
+    pos = rng.integers(1, 30000, T).astype(np.int32)
+    out = oracle.qk_norm_rope(x, w, pos, ROPE_BASE)
+    normed = F.rms_norm(torch.from_numpy(x.astype(np.float64)), (D,),
+                        torch.from_numpy(w.astype(np.float64)), eps=1e-6).numpy()
+    ref = _complex_turn(normed, pos.astype(np.float64), _recovered_freqs(D, ROPE_BASE))
+    np.testing.assert_allclose(out, ref, atol=1e-9)
+    wrong_order = _complex_turn(x.astype(np.float64), pos.astype(np.float64),
+                                _recovered_freqs(D, ROPE_BASE))
+    wrong_order = F.rms_norm(torch.from_numpy(wrong_order), (D,),
+                             torch.from_numpy(w.astype(np.float64)), eps=1e-6).numpy()
+    assert np.abs(out - wrong_order).max() > 0.1
