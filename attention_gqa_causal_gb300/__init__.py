@@ -5,6 +5,10 @@ Two hot paths behind a C ABI (include/attn.h, libattn_gb300.so):
 * ``attn_prefill``      causal / full GQA prefill on tcgen05 tensor cores
 * ``attn_decode_paged`` single-token decode over a paged KV cache
   (split-K main kernel + log-sum-exp combine kernel)
+* ``attn_prefill_paged`` chunked prefill of new query chunks over the paged
+  cache (cached prefixes, ragged lengths)
+* ``attn_kv_append`` / ``attn_qk_norm_rope(_append)`` the attention-input
+  prologue: KV append, per-head QK-norm and NeoX RoPE
 
 This package is the thin Python binding: PyTorch provides device memory and
 streams, the library does all of the work.
@@ -31,8 +35,12 @@ from ._binding import (  # noqa: F401
     attn_lse_combine,
     attn_prefill,
     attn_prefill_paged,
+    attn_qk_norm_rope,
+    attn_qk_norm_rope_append,
+    attn_rope_cos_sin_table,
     attn_release_workspace,
     attn_version,
     load,
+    rope_table_entries,
     status_string,
 )

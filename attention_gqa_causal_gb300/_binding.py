@@ -27,7 +27,8 @@ EXPORTED = [
     "attn_decode_paged_ws", "attn_lse_combine", "attn_release_workspace",
     "attn_get_device_error", "attn_last_cuda_error", "attn_status_string", "attn_version",
     "attn_decode_paged_noalloc", "attn_debug_prefill_stall", "attn_kv_append",
-    "attn_decode_paged_append", "attn_prefill_paged",
+    "attn_decode_paged_append", "attn_prefill_paged", "attn_rope_cos_sin_table",
+    "attn_qk_norm_rope", "attn_qk_norm_rope_append",
 ]
 
 # Size of the scratch buffer compiled into the library for attn_decode_paged_noalloc.
@@ -73,6 +74,11 @@ def load():
             lib.attn_decode_paged_append.argtypes = [p, p, p, p, p, p, p, p, p, i, i, i, i, i, i,
                                                      ll, p]
             lib.attn_prefill_paged.argtypes = [p, p, p, p, p, p, p, i, i, i, i, i, i, i, i, ll, i, p]
+            f, d = ctypes.c_float, ctypes.c_double
+            lib.attn_rope_cos_sin_table.argtypes = [p, i, i, d, p]
+            lib.attn_qk_norm_rope.argtypes = [p, p, p, p, p, i, p, i, i, i, i, f, p]
+            lib.attn_qk_norm_rope_append.argtypes = [p, p, p, p, p, p, i, p, p, p, p, i, i, i, i, i,
+                                                     ll, f, p]
             _lib = lib
     return _lib
 
@@ -204,6 +210,79 @@ def attn_decode_paged_append(q, k_new, v_new, k_cache, v_cache, out, slot_mappin
     _check(load().attn_decode_paged_append(ptrs[0], extra[0], extra[1], ptrs[1], ptrs[2], ptrs[3],
                                            extra[2], ptrs[4], ptrs[5], *sizes, k_cache.shape[0],
                                            ctypes.c_void_p(st)), "attn_decode_paged_append")
+
+
+def attn_rope_cos_sin_table(cos_sin: torch.Tensor, base: float, stream=None) -> None:
+    """Fill cos_sin [max_pos, 128] FP32 with the rotary table: the (cos, sin) of
+    p * base^(-2j/128) for every position p and pair j, computed in FP64 on the
+    device and rounded once, in the entry order include/attn.h documents
+    (rope_table_entries() gives the plain [max_pos, 64] cos and sin)."""
+    if cos_sin.dim() != 2 or cos_sin.shape[1] != 128:
+        raise ValueError("expected cos_sin [max_pos, 128] float32")
+    ptr = _dev(cos_sin, "cos_sin", torch.float32)
+    st = _stream(stream, cos_sin.device)
+    _check(load().attn_rope_cos_sin_table(ptr, cos_sin.shape[0], 128, float(base), ctypes.c_void_p(st)),
+           "attn_rope_cos_sin_table")
+
+
+def rope_table_entries(cos_sin):
+    """(cos, sin), each [max_pos, 64] in pair order, from a table filled by
+    attn_rope_cos_sin_table: entry (p, i, m) = p*32 + i*8 + m of its float4
+    view holds {cos j, cos j+1, sin j, sin j+1} for pair j = 8m + 2i."""
+    t = cos_sin.reshape(-1, 4, 8, 4)                 # [p, i, m, 4]
+    j_even = t[..., [0, 2]].permute(0, 2, 1, 3)      # [p, m, i, (cos, sin)] of pair 8m+2i
+    j_odd = t[..., [1, 3]].permute(0, 2, 1, 3)       # pair 8m+2i+1
+    pairs = torch.stack([j_even, j_odd], dim=3).reshape(t.shape[0], 64, 2)
+    return pairs[..., 0], pairs[..., 1]
+
+
+def _prologue_args(Q, K, q_weight, k_weight, cos_sin, positions):
+    if Q.dim() != 3 or K.dim() != 3 or K.shape[0] != Q.shape[0] or K.shape[2] != Q.shape[2]:
+        raise ValueError("expected Q [T,H_q,D] and K [T,H_kv,D]")
+    if cos_sin.dim() != 2 or cos_sin.shape[1] != Q.shape[2]:
+        raise ValueError("expected cos_sin [max_pos, D] float32")
+    if positions.shape != (Q.shape[0],):
+        raise ValueError("expected positions [T] int32")
+    w = []
+    for name, t in (("q_weight", q_weight), ("k_weight", k_weight)):
+        if t is None:
+            w.append(None)
+        else:
+            if t.shape != (Q.shape[2],):
+                raise ValueError(f"expected {name} [D]")
+            w.append(_dev(t, name, torch.float16))
+    return w, _dev(cos_sin, "cos_sin", torch.float32), _dev(positions, "positions", torch.int32)
+
+
+def attn_qk_norm_rope(Q, K, q_weight, k_weight, cos_sin, positions, eps: float = 1e-6,
+                      stream=None) -> None:
+    """In place: per-head RMSNorm (weight None = none) then NeoX RoPE of
+    Q [T,H_q,128] and K [T,H_kv,128] at positions [T]."""
+    w, cs, pos = _prologue_args(Q, K, q_weight, k_weight, cos_sin, positions)
+    T, H_q, D = Q.shape
+    st = _stream(stream, Q.device)
+    _check(load().attn_qk_norm_rope(_dev(Q, "Q", torch.float16), _dev(K, "K", torch.float16),
+                                    w[0], w[1], cs, cos_sin.shape[0], pos, T, H_q, K.shape[1], D,
+                                    float(eps), ctypes.c_void_p(st)), "attn_qk_norm_rope")
+
+
+def attn_qk_norm_rope_append(Q, K, V, q_weight, k_weight, cos_sin, positions, slot_mapping,
+                             k_cache, v_cache, eps: float = 1e-6, stream=None) -> None:
+    """Q normalised and rotated in place; K normalised and rotated, and V as is,
+    written to their paged slots (int64 slot_mapping, -1 skipped)."""
+    w, cs, pos = _prologue_args(Q, K, q_weight, k_weight, cos_sin, positions)
+    T, H_q, D = Q.shape
+    if V.shape != K.shape or k_cache.dim() != 4 or v_cache.shape != k_cache.shape:
+        raise ValueError("expected V like K and caches [num_blocks,H_kv,block_size,D]")
+    if slot_mapping.shape != (T,):
+        raise ValueError("expected slot_mapping [T]")
+    st = _stream(stream, Q.device)
+    _check(load().attn_qk_norm_rope_append(
+        _dev(Q, "Q", torch.float16), _dev(K, "K", torch.float16), _dev(V, "V", torch.float16),
+        w[0], w[1], cs, cos_sin.shape[0], pos, _dev(slot_mapping, "slot_mapping", torch.int64),
+        _dev(k_cache, "k_cache", torch.float16), _dev(v_cache, "v_cache", torch.float16), T, H_q,
+        K.shape[1], D, k_cache.shape[2], k_cache.shape[0], float(eps), ctypes.c_void_p(st)),
+        "attn_qk_norm_rope_append")
 
 
 def attn_decode_paged_workspace_bytes(num_seqs: int, H_q: int, H_kv: int, D: int,

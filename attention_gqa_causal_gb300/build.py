@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libattn_gb300.so")
-SOURCES = ["api.cu", "decode.cu", "prefill.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "decode.cu", "prefill.cu", "noalloc.cu", "rope.cu"]
 HEADERS = ["ptx.cuh", "internal.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -1,6 +1,7 @@
 // api.cu -- the C ABI of libattn_gb300: argument validation, workspace
 // ownership, error mapping.  Every compute step runs in the kernels of
-// prefill.cu and decode.cu.
+// prefill.cu, decode.cu and rope.cu.
+#include <cmath>
 #include <cstdint>
 #include <map>
 #include <mutex>
@@ -275,6 +276,108 @@ ATTN_API int attn_lse_combine(const float* O_part, const float* lse, void* out, 
     if (!O_part || !lse || !out || !aligned(O_part, 16) || !aligned(lse, 4) || !aligned(out, 16))
         return ATTN_ERR_INVALID_ARG;
     const cudaError_t e = attn::launch_lse_combine(O_part, lse, out, R, n_split, stream);
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+ATTN_API int attn_rope_cos_sin_table(float* cos_sin, int max_pos, int D, double base,
+                                     cudaStream_t stream)
+{
+    if (max_pos < 0 || !(base > 0.0) || !std::isfinite(base))
+        return ATTN_ERR_INVALID_ARG;
+    if (D != attn::kHeadDim)
+        return ATTN_ERR_UNSUPPORTED;
+    if (max_pos == 0)
+        return ATTN_OK;
+    if (!cos_sin || !aligned(cos_sin, 16))
+        return ATTN_ERR_INVALID_ARG;
+    const cudaError_t e = attn::launch_rope_table(cos_sin, max_pos, base, stream);
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+namespace {
+
+// Checks shared by both prologue entry points.
+int validate_prologue(const void* Q, const void* K, const void* q_weight, const void* k_weight,
+                      const float* cos_sin, int max_pos, const int* positions, int num_tokens,
+                      int H_q, int H_kv, int D, float eps)
+{
+    if (num_tokens < 0 || H_q < 1 || H_kv < 1 || max_pos < 1 || !(eps >= 0.0f) || !std::isfinite(eps))
+        return ATTN_ERR_INVALID_ARG;
+    if (D != attn::kHeadDim)
+        return ATTN_ERR_UNSUPPORTED;
+    if (num_tokens == 0)
+        return ATTN_OK;
+    if (!Q || !K || !cos_sin || !positions || !aligned(Q, 16) || !aligned(K, 16) ||
+        !aligned(cos_sin, 16) || !aligned(positions, 4) || !aligned(q_weight, 16) ||
+        !aligned(k_weight, 16))
+        return ATTN_ERR_INVALID_ARG;
+    const size_t qb = (size_t)num_tokens * H_q * D * 2, kb = (size_t)num_tokens * H_kv * D * 2;
+    const size_t tb = (size_t)max_pos * D / 2 * sizeof(float) * 2, pb = (size_t)num_tokens * 4;
+    const void* read_only[] = {q_weight, k_weight, cos_sin, positions};
+    const size_t ro_bytes[] = {(size_t)D * 2, (size_t)D * 2, tb, pb};
+    if (overlap(Q, qb, K, kb))
+        return ATTN_ERR_INVALID_ARG;
+    for (int i = 0; i < 4; i++)
+        if (read_only[i] && (overlap(Q, qb, read_only[i], ro_bytes[i]) ||
+                             overlap(K, kb, read_only[i], ro_bytes[i])))
+            return ATTN_ERR_INVALID_ARG;
+    return ATTN_OK;
+}
+
+}  // namespace
+
+ATTN_API int attn_qk_norm_rope(void* Q, void* K, const void* q_weight, const void* k_weight,
+                               const float* cos_sin, int max_pos, const int* positions,
+                               int num_tokens, int H_q, int H_kv, int D, float eps,
+                               cudaStream_t stream)
+{
+    const int v = validate_prologue(Q, K, q_weight, k_weight, cos_sin, max_pos, positions,
+                                    num_tokens, H_q, H_kv, D, eps);
+    if (v != ATTN_OK || num_tokens == 0)
+        return v;
+    if (H_q + H_kv > attn::kMaxPrologueRowsPerToken)
+        return ATTN_ERR_UNSUPPORTED;
+    const cudaError_t e = attn::launch_qk_norm_rope(Q, K, nullptr, K, q_weight, k_weight, cos_sin,
+                                                    max_pos, positions, nullptr, nullptr, nullptr, 0,
+                                                    num_tokens, H_q, H_kv, eps, stream);
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+ATTN_API int attn_qk_norm_rope_append(void* Q, const void* K, const void* V, const void* q_weight,
+                                      const void* k_weight, const float* cos_sin, int max_pos,
+                                      const int* positions, const long long* slot_mapping,
+                                      void* k_cache, void* v_cache, int num_tokens, int H_q,
+                                      int H_kv, int D, int block_size, long long num_blocks,
+                                      float eps, cudaStream_t stream)
+{
+    const int v = validate_prologue(Q, K, q_weight, k_weight, cos_sin, max_pos, positions,
+                                    num_tokens, H_q, H_kv, D, eps);
+    if (v != ATTN_OK)
+        return v;
+    if (block_size != attn::kPageSize || H_q + 2 * H_kv > attn::kMaxPrologueRowsPerToken)
+        return ATTN_ERR_UNSUPPORTED;
+    if (num_blocks < 0)
+        return ATTN_ERR_INVALID_ARG;
+    if (num_tokens == 0)
+        return ATTN_OK;
+    if (!V || !slot_mapping || !k_cache || !v_cache || !aligned(V, 16) || !aligned(slot_mapping, 8) ||
+        !aligned(k_cache, 16) || !aligned(v_cache, 16))
+        return ATTN_ERR_INVALID_ARG;
+    const size_t qb = (size_t)num_tokens * H_q * D * 2, kb = (size_t)num_tokens * H_kv * D * 2;
+    const size_t cb = (size_t)num_blocks * H_kv * block_size * D * 2;
+    if (overlap(Q, qb, V, kb) || overlap(k_cache, cb, v_cache, cb))
+        return ATTN_ERR_INVALID_ARG;
+    const void* inputs[] = {Q, K, V, cos_sin, positions, slot_mapping, q_weight, k_weight};
+    const size_t in_bytes[] = {qb, kb, kb, (size_t)max_pos * D * 4, (size_t)num_tokens * 4,
+                               (size_t)num_tokens * 8, (size_t)D * 2, (size_t)D * 2};
+    for (int i = 0; i < 8; i++)
+        if (inputs[i] && (overlap(k_cache, cb, inputs[i], in_bytes[i]) ||
+                          overlap(v_cache, cb, inputs[i], in_bytes[i])))
+            return ATTN_ERR_INVALID_ARG;
+    const cudaError_t e = attn::launch_qk_norm_rope(Q, K, V, nullptr, q_weight, k_weight, cos_sin,
+                                                    max_pos, positions, slot_mapping, k_cache,
+                                                    v_cache, num_blocks, num_tokens, H_q, H_kv,
+                                                    eps, stream);
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
 

@@ -9,6 +9,8 @@ namespace attn {
 
 constexpr int kHeadDim = 128;   // the only head_dim the kernels are built for
 constexpr int kPageSize = 16;   // the only KV block size the kernels are built for
+// The prologue stages whole tokens (all their q, k and v rows) in shared memory.
+constexpr int kMaxPrologueRowsPerToken = 192;
 
 // Device error word bits (set by kernels, read by attn_get_device_error).
 enum DeviceError : int {
@@ -19,6 +21,7 @@ enum DeviceError : int {
     kDevErrSmemLayout = 16,    // dynamic shared memory base too misaligned for the tile layout
     kDevErrBadSlot = 32,       // a slot_mapping entry outside [-1, num_blocks * block_size)
     kDevErrBadLengths = 64,    // paged prefill: a chunk longer than its context (L_q > L_kv)
+    kDevErrBadPosition = 128,  // prologue: a position outside [0, max_pos) of the cos/sin table
 };
 
 // Set by the kernels (atomicOr); defined in decode.cu.  Device address of the
@@ -75,5 +78,20 @@ cudaError_t launch_prefill_paged(const void* Q, const void* k_cache, const void*
                                  const int* block_tables, int B, int max_seqlen_q, int total_q,
                                  int H_q, int H_kv, int max_blocks_per_seq, long long num_blocks,
                                  int causal, cudaStream_t stream);
+
+// The rotary table: per position 32 float4, entry p*32 + i*8 + m holding
+// {cos a, cos b, sin a, sin b} of the angles p * base^(-2j/128) of pairs
+// a = 8m + 2i and b = a + 1; computed in FP64, rounded to FP32.
+cudaError_t launch_rope_table(float* cos_sin, int max_pos, double base, cudaStream_t stream);
+
+// Per-head RMSNorm (weights q_w / k_w, nullptr = none) then NeoX RoPE of q
+// [T, H_q, 128] (in place) and k [T, H_kv, 128].  Without k_cache, k goes to
+// k_out (may equal k); with k_cache, k and v go to the paged slots of
+// slot_mapping (-1 skipped) and k_out is unused.
+cudaError_t launch_qk_norm_rope(void* q, const void* k, const void* v, void* k_out,
+                                const void* q_w, const void* k_w, const float* cos_sin,
+                                int max_pos, const int* positions, const long long* slot_mapping,
+                                void* k_cache, void* v_cache, long long num_blocks, int T,
+                                int H_q, int H_kv, float eps, cudaStream_t stream);
 
 }  // namespace attn

@@ -11,6 +11,8 @@ One step is one pass over every hot-path kernel on its workload:
   * paged decode          8 sequences x 32768 tokens, H 16/8
   * the 256-sequence decode step together with its KV append (two launches)
     (decode: GB/s of K/V bytes of the valid tokens; split-K + combine kernels)
+  * the attention-input prologue (QK-norm, RoPE, KV append) of 2 x 8192 new
+    tokens, H 32/8 (GB/s of the bytes it must move)
 Each kernel launch is bracketed by CUDA events on the stream it runs on; the
 K timed steps are bracketed by a barrier and a device synchronisation.  All
 inputs are resident in HBM and larger than L2 (129 MB), so no flush is done.
@@ -45,6 +47,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 KERNEL_SOURCES = {
     "prefill_kernel": ["prefill.cu", "ptx.cuh"],
     "decode_splitk_kernel": ["decode.cu"],
+    "qk_norm_rope_kernel": ["rope.cu", "ptx.cuh"],
 }
 
 
@@ -221,6 +224,29 @@ def build_legs(torch, ag, which):
             leg2.dev_in, leg2.dev_out = tuple(t) + (dkn, dvn, dsl), out
             leg2.config = dict(leg.config, append_bytes=app_bytes)
             legs.append(leg2)
+    if which in ("all", "prologue"):
+        # QK-norm + RoPE + KV append of the prefill workload's 2 x 8192 new tokens:
+        # q rotated in place (repeated steps re-normalise it, so values stay bounded),
+        # k and v written to a permutation of the cache slots.  Last in the step:
+        # the ~100 MB it leaves dirty in L2 are written back during the next
+        # (compute-bound) prefill rather than during a bandwidth-bound decode.
+        cfg = W.PROLOGUE
+        Q, K, V, qw, kw, pos, slots, nb = W.prologue_inputs(cfg, seed=0)
+        t = [torch.from_numpy(x).cuda() for x in (Q, K, V, qw, kw, pos, slots)]
+        kc = torch.zeros((nb, cfg.H_kv, 16, cfg.D), dtype=torch.float16, device="cuda")
+        vc = torch.zeros_like(kc)
+        cs = torch.empty((cfg.seq_len, cfg.D), dtype=torch.float32, device="cuda")
+        ag.attn_rope_cos_sin_table(cs, cfg.base)
+        leg = Leg(cfg.name, "prologue", cfg.bytes(), "GB/s", 1)
+        leg.run = (lambda t=t, kc=kc, vc=vc, cs=cs: ag.attn_qk_norm_rope_append(
+            t[0], t[1], t[2], t[3], t[4], cs, t[5], t[6], kc, vc, eps=1e-6))
+        leg.host = {"Q": Q, "K": K, "V": V, "q_weight": qw, "k_weight": kw, "positions": pos,
+                    "slot_mapping": slots}
+        leg.dev_in, leg.dev_out = tuple(t), t[0]
+        leg.config = {"tokens": cfg.tokens, "seq_len": cfg.seq_len, "H_q": cfg.H_q,
+                      "H_kv": cfg.H_kv, "D": cfg.D, "rope_base": cfg.base, "eps": 1e-6,
+                      "block_size": 16, "num_blocks": nb, "bytes": cfg.bytes()}
+        legs.append(leg)
     return legs
 
 
@@ -347,10 +373,11 @@ def run_ours(args):
                                 "traffic": dram_traffic("prefill_kernel", leg.name)}
         else:
             peak = peaks["hbm_gbs"]
+            kernel = "qk_norm_rope_kernel" if leg.kind == "prologue" else "decode_splitk_kernel"
             part["roofline"] = {"bound": "hbm", "achieved": leg.value(ms), "peak": peak,
                                 "unit": "GB/s", "frac": leg.value(ms) / peak,
                                 "peak_kind": f"{peak_src} copy bandwidth",
-                                "traffic": dram_traffic("decode_splitk_kernel", leg.name)}
+                                "traffic": dram_traffic(kernel, leg.name)}
         parts.append(part)
 
     e2e = None
@@ -427,7 +454,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["all", "prefill", "prefill_full", "prefill_paged", "decode",
+    ap.add_argument("--workload", choices=["all", "prefill", "prefill_full", "prefill_paged", "prologue", "decode",
                                            "decode_long", "decode_append"],
                     default="all")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,

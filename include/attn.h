@@ -212,6 +212,63 @@ ATTN_API int attn_decode_paged_append(const void* q, const void* k_new, const vo
                                       cudaStream_t stream);
 
 /*
+ * Attention-input prologue, step 1: the rotary cos/sin table.  Pair j
+ * (element j with element j + D/2, j < D/2) turns by a_j(p) = p * base^(-2j/D)
+ * at position p (the angle of the Kimi-K2.6 KernelBench trace, fused
+ * cross-attention page); the FP32 table indexed by position is the "RoPE
+ * design" of the "GRPO-CUDA Project Memory" page.  The buffer holds max_pos*D
+ * floats (16-byte aligned, caller-owned): per position 512 bytes, ordered for
+ * the prologue kernel's loads as float4 entries
+ *   cos_sin[(p*32 + i*8 + m)*4 + 0..3] = {cos a_j, cos a_j+1, sin a_j, sin a_j+1},
+ *   j = 8m + 2i,  m < 8,  i < 4.
+ * The angles and their sines and cosines are computed in FP64 and rounded
+ * once, so late positions lose no accuracy.  D must be 128; base > 0 (the
+ * pages print no value: it is the model's RoPE base).  Build it once.
+ */
+ATTN_API int attn_rope_cos_sin_table(float* cos_sin, int max_pos, int D, double base,
+                                     cudaStream_t stream);
+
+/*
+ * Attention-input prologue, step 2, in place: per-head QK-norm then NeoX RoPE
+ * ("GRPO-CUDA Project Memory" page, "Qwen3-Specific Notes": RMSNorm over each
+ * head's 128 values before RoPE, eps 1e-6 there; "RoPE design": element i
+ * rotates with element i + D/2):
+ *   y = w * x / sqrt(mean(x^2) + eps)              (no norm when w is NULL)
+ *   x'[i] = y[i] c - y[i+64] s,  x'[i+64] = y[i+64] c + y[i] s,
+ *   (c, s) = (cos, sin) of pair i at positions[t], from the table above
+ * Q         : [num_tokens, H_q, D] FP16, rewritten in place
+ * K         : [num_tokens, H_kv, D] FP16, rewritten in place
+ * q_weight, k_weight : [D] FP16 RMSNorm weights, or NULL for RoPE only
+ * cos_sin   : the table of attn_rope_cos_sin_table, max_pos positions
+ * positions : [num_tokens] int32, each token's absolute position
+ * FP32 arithmetic, FP16 results rounded to nearest.  D must be 128 and
+ * H_q + H_kv at most 192 (ATTN_ERR_UNSUPPORTED otherwise).  A token whose
+ * position lies outside [0, max_pos) is left unchanged and flagged in the
+ * device error word (bit 128, ATTN_ERR_BAD_INPUT).  Q and K must not overlap
+ * each other or the read-only inputs.  One launch.
+ */
+ATTN_API int attn_qk_norm_rope(void* Q, void* K, const void* q_weight, const void* k_weight,
+                               const float* cos_sin, int max_pos, const int* positions,
+                               int num_tokens, int H_q, int H_kv, int D, float eps,
+                               cudaStream_t stream);
+
+/*
+ * The prologue fused with the KV append, in the page's layer order (QK-norm,
+ * RoPE, KV append, then attention: "Model forward pass"): Q is normalised and
+ * rotated in place as in attn_qk_norm_rope; K is normalised and rotated and V
+ * copied straight into their paged cache slots (attn_kv_append's slot rules:
+ * slot -1 skipped, out-of-range flagged with bit 32); K and V themselves are
+ * only read.  Caches [num_blocks, H_kv, block_size, D] FP16, block_size 16,
+ * must not overlap any input; H_q + 2*H_kv at most 192.  One launch.
+ */
+ATTN_API int attn_qk_norm_rope_append(void* Q, const void* K, const void* V, const void* q_weight,
+                                      const void* k_weight, const float* cos_sin, int max_pos,
+                                      const int* positions, const long long* slot_mapping,
+                                      void* k_cache, void* v_cache, int num_tokens, int H_q,
+                                      int H_kv, int D, int block_size, long long num_blocks,
+                                      float eps, cudaStream_t stream);
+
+/*
  * Merge partial attention results over disjoint key segments by their
  * log-sum-exp (the combine step of split-K decode):
  *   L = log sum_i exp(lse[r,i]),  out[r,:] = sum_i exp(lse[r,i] - L) O_part[r,i,:]
@@ -232,7 +289,7 @@ ATTN_API int attn_release_workspace(void);
  * *code receives the raw bits (1 timeout, 2 negative block id, 4 seq_len
  * beyond the table, 16 shared-memory layout did not fit, 32 slot out of
  * range, 64 a paged-prefill chunk longer than its context or than
- * max_seqlen_q); the return is ATTN_OK if it is 0, else ATTN_ERR_TIMEOUT
+ * max_seqlen_q, 128 a prologue position outside the cos/sin table); the return is ATTN_OK if it is 0, else ATTN_ERR_TIMEOUT
  * or ATTN_ERR_BAD_INPUT.  reset != 0 clears it.
  */
 ATTN_API int attn_get_device_error(int* code, int reset);

@@ -162,3 +162,71 @@ def test_prefill_paged_validation():
     assert pp(O=A16 + 64) == ag.ATTN_ERR_INVALID_ARG          # O overlaps Q
     assert pp(O=A16B + 128) == ag.ATTN_ERR_INVALID_ARG        # O overlaps the K cache
     assert pp(B=0) == ag.ATTN_OK and pp(tq=0) == ag.ATTN_OK and pp(mq=0) == ag.ATTN_OK
+
+
+def test_rope_table_validation():
+    lib = ag.load()
+    D = ctypes.c_double
+    assert lib.attn_rope_cos_sin_table(P(A16), 100, 64, D(1e4), P(0)) == ag.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_rope_cos_sin_table(P(A16), -1, 128, D(1e4), P(0)) == ag.ATTN_ERR_INVALID_ARG
+    assert lib.attn_rope_cos_sin_table(P(A16), 100, 128, D(0.0), P(0)) == ag.ATTN_ERR_INVALID_ARG
+    assert lib.attn_rope_cos_sin_table(P(A16), 100, 128, D(float("inf")), P(0)) == ag.ATTN_ERR_INVALID_ARG
+    assert lib.attn_rope_cos_sin_table(P(MIS), 100, 128, D(1e4), P(0)) == ag.ATTN_ERR_INVALID_ARG
+    assert lib.attn_rope_cos_sin_table(P(0), 100, 128, D(1e4), P(0)) == ag.ATTN_ERR_INVALID_ARG
+    assert lib.attn_rope_cos_sin_table(P(A16), 0, 128, D(1e4), P(0)) == ag.ATTN_OK
+
+
+def test_qk_norm_rope_validation():
+    lib = ag.load()
+    F = ctypes.c_float
+    # Q 4 tokens x 8 heads x 256 B = 8 KB at A16; K 4 KB at A16 + 0x4000
+    base = dict(Q=A16, K=A16 + 0x4000, qw=A16 + 0x8000, kw=A16 + 0x8100, cs=A16 + 0x10000,
+                mp=64, pos=A16 + 0x20000, T=4, Hq=8, Hkv=4, D=128, eps=1e-6)
+
+    def qr(**kw):
+        a = dict(base, **kw)
+        return lib.attn_qk_norm_rope(P(a["Q"]), P(a["K"]), P(a["qw"]), P(a["kw"]), P(a["cs"]), a["mp"],
+                                     P(a["pos"]), a["T"], a["Hq"], a["Hkv"], a["D"], F(a["eps"]), P(0))
+
+    assert qr(D=64) == ag.ATTN_ERR_UNSUPPORTED
+    assert qr(T=-1) == ag.ATTN_ERR_INVALID_ARG
+    assert qr(Hkv=0) == ag.ATTN_ERR_INVALID_ARG
+    assert qr(mp=0) == ag.ATTN_ERR_INVALID_ARG
+    assert qr(eps=-1.0) == ag.ATTN_ERR_INVALID_ARG
+    assert qr(eps=float("nan")) == ag.ATTN_ERR_INVALID_ARG
+    assert qr(pos=0) == ag.ATTN_ERR_INVALID_ARG
+    assert qr(cs=MIS) == ag.ATTN_ERR_INVALID_ARG                  # table must be 16-byte aligned
+    assert qr(qw=A16 + 0x8008) == ag.ATTN_ERR_INVALID_ARG         # weight must be 16-byte aligned
+    assert qr(K=A16 + 0x1000) == ag.ATTN_ERR_INVALID_ARG          # K overlaps Q
+    assert qr(qw=A16 + 0x100) == ag.ATTN_ERR_INVALID_ARG          # a weight inside Q
+    assert qr(cs=A16 + 0x1000) == ag.ATTN_ERR_INVALID_ARG         # the table inside Q
+    assert qr(Q=A16B, Hq=190, Hkv=3) == ag.ATTN_ERR_UNSUPPORTED   # more than 192 rows per token
+    assert qr(T=0) == ag.ATTN_OK
+    assert qr(T=0, qw=0, kw=0) == ag.ATTN_OK                      # null weights are allowed
+
+
+def test_qk_norm_rope_append_validation():
+    lib = ag.load()
+    F, LL = ctypes.c_float, ctypes.c_longlong
+    base = dict(Q=A16, K=A16 + 0x4000, V=A16 + 0x6000, qw=A16 + 0x8000, kw=A16 + 0x8100,
+                cs=A16 + 0x10000, mp=64, pos=A16 + 0x20000, sm=A16 + 0x20100, kc=A16B,
+                vc=A16B + 0x1000000, T=4, Hq=8, Hkv=4, D=128, bs=16, nb=16, eps=1e-6)
+
+    def qa(**kw):
+        a = dict(base, **kw)
+        return lib.attn_qk_norm_rope_append(
+            P(a["Q"]), P(a["K"]), P(a["V"]), P(a["qw"]), P(a["kw"]), P(a["cs"]), a["mp"], P(a["pos"]),
+            P(a["sm"]), P(a["kc"]), P(a["vc"]), a["T"], a["Hq"], a["Hkv"], a["D"], a["bs"], LL(a["nb"]),
+            F(a["eps"]), P(0))
+
+    assert qa(D=64) == ag.ATTN_ERR_UNSUPPORTED
+    assert qa(bs=32) == ag.ATTN_ERR_UNSUPPORTED
+    assert qa(nb=-1) == ag.ATTN_ERR_INVALID_ARG
+    assert qa(V=0) == ag.ATTN_ERR_INVALID_ARG
+    assert qa(sm=A16 + 0x20104) == ag.ATTN_ERR_INVALID_ARG         # slot_mapping must be 8-byte aligned
+    assert qa(V=A16 + 0x1000) == ag.ATTN_ERR_INVALID_ARG          # V overlaps Q
+    assert qa(kc=A16) == ag.ATTN_ERR_INVALID_ARG                  # cache overlaps Q
+    assert qa(vc=A16B + 0x100) == ag.ATTN_ERR_INVALID_ARG         # the two caches overlap
+    assert qa(vc=A16 + 0x10000) == ag.ATTN_ERR_INVALID_ARG        # cache over the cos/sin table
+    assert qa(Q=A16B + 0x4000000, Hq=180, Hkv=7) == ag.ATTN_ERR_UNSUPPORTED   # 194 rows per token
+    assert qa(T=0) == ag.ATTN_OK

@@ -237,3 +237,49 @@ def chunked_prefill_inputs(cfg: ChunkedPrefillConfig, seed: int = 0):
     Q = normal_fp16(seed, 0, (cfg.num_seqs * cfg.chunk, cfg.H_q, cfg.D))
     cu = np.arange(0, (cfg.num_seqs + 1) * cfg.chunk, cfg.chunk, dtype=np.int32)
     return Q, kc, vc, cu, lens_kv, tables
+
+
+@dataclass(frozen=True)
+class PrologueConfig:
+    """The attention-input prologue (QK-norm, RoPE, KV append) over the new
+    tokens of num_seqs sequences of seq_len tokens, at positions 0..seq_len-1."""
+    name: str
+    num_seqs: int
+    seq_len: int
+    H_q: int
+    H_kv: int
+    D: int = 128
+    base: float = 1.0e6     # RoPE base; the pages print none (Qwen3 models use 1e6)
+
+    @property
+    def tokens(self) -> int:
+        return self.num_seqs * self.seq_len
+
+    def bytes(self) -> float:
+        """HBM bytes the op must move: each token's q, k and v rows read once
+        and written once (q in place, k and v to their cache slots), plus its
+        64 (cos, sin) FP32 pairs, its int32 position and its int64 slot."""
+        row = self.D * 2
+        per_token = 2 * row * (self.H_q + 2 * self.H_kv) + (self.D // 2) * 8 + 4 + 8
+        return float(per_token * self.tokens)
+
+
+PROLOGUE = PrologueConfig("qk_norm_rope_append_b2_s8192_h32_kv8", 2, 8192, 32, 8)
+
+
+def prologue_inputs(cfg: PrologueConfig, seed: int = 0):
+    """Q [T, H_q, D] and K, V [T, H_kv, D] (streams 10-12), RMSNorm weights
+    1 + N(0, 1)/4 (streams 13/14), positions 0..seq_len-1 per sequence, and
+    each token's cache slot from a seeded permutation of ceil(T/16)*16 slots
+    (stream 15).  Returns (Q, K, V, q_weight, k_weight, positions, slots,
+    num_blocks)."""
+    T = cfg.tokens
+    Q = normal_fp16(seed, 10, (T, cfg.H_q, cfg.D))
+    K = normal_fp16(seed, 11, (T, cfg.H_kv, cfg.D))
+    V = normal_fp16(seed, 12, (T, cfg.H_kv, cfg.D))
+    qw = (1.0 + 0.25 * normal_fp16(seed, 13, (cfg.D,)).astype(np.float32)).astype(np.float16)
+    kw = (1.0 + 0.25 * normal_fp16(seed, 14, (cfg.D,)).astype(np.float32)).astype(np.float16)
+    positions = np.tile(np.arange(cfg.seq_len, dtype=np.int32), cfg.num_seqs)
+    num_blocks = (T + 15) // 16
+    slots = permutation(seed, 15, num_blocks * 16)[:T].astype(np.int64)
+    return Q, K, V, qw, kw, positions, slots, num_blocks
