@@ -393,7 +393,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             const int sk1 = (j + 1) % kKStages;
             const uint32_t phk1 = ((j + 1) / kKStages) & 1;
             const bool more = j + 1 < w.n_kv;
-            ok = wait(ctl.p_full[0], j & 1) && wait(ctl.v_full[sv], phv);
+            // Operands first (usually long in place: the warp is idle until tile 0's
+            // P is ready anyway), so that nothing stands between PV0 and S0 below:
+            // each mbarrier wait costs the issuing warp of order a hundred cycles.
+            ok = wait(ctl.v_full[sv], phv) && (!more || wait(ctl.k_full[sk1], phk1)) &&
+                 wait(ctl.p_full[0], j & 1);
             if (!ok)
                 break;
             if (PAGED && (j + 1) * BN > w.Lkv) {
@@ -417,19 +421,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 issue_o(0, sv, j > 0);
                 if (!more)
                     mma_commit(smem_u32(&ctl.o_full[0]));
-            }
-            __syncwarp();
-            if (more) {
-                ok = wait(ctl.k_full[sk1], phk1);
-                if (!ok)
-                    break;
-                tc_fence_after();
-                if (leader) {
+                else {
                     issue_s(0, sk1);
                     mma_commit(smem_u32(&ctl.s_full[0]));
                 }
-                __syncwarp();
             }
+            __syncwarp();
             ok = wait(ctl.p_full[1], j & 1);
             if (!ok)
                 break;
