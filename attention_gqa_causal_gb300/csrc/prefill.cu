@@ -64,7 +64,17 @@ constexpr int D = kHeadDim;
 constexpr int kPagesPerTile = BN / kPageSize;
 constexpr int kMmaWarp = 8;
 constexpr int kTmaWarp = 9;
-constexpr int kThreads = 10 * 32;
+constexpr int kThreads = 12 * 32;   // warps 10, 11 only complete the third warpgroup
+// Registers per thread after the warpgroups re-balance (setmaxnreg): the MMA/TMA
+// warpgroup gives up what the softmax needs to keep a whole 128-key row of S
+// in flight (at 168 registers its exp loop serialises).  Launch pool: 384
+// threads x 168 = 64512 >= 256 x kSoftmaxRegs + 128 x kControlRegs = 63488,
+// and per SM sub-partition (3 warps) 200 + 200 + 96 <= 512.  The host checks
+// the compiled register count before launching (an increase that the pool
+// cannot cover would wait forever).
+constexpr int kSoftmaxRegs = 200;
+constexpr int kControlRegs = 96;
+static_assert(256 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * 168, "register re-balance exceeds the launch pool");
 constexpr int kKStages = 2;
 constexpr int kVStages = 3;
 constexpr uint32_t kTileBytes = BM * D * 2;      // 32 KB
@@ -174,6 +184,18 @@ constexpr uint32_t kSmemAlloc = kSmemMax;
 constexpr uint32_t kAlignSlack = kSmemMax - kSmemBytes - (uint32_t)sizeof(SmemCtl);
 static_assert(kSmemBytes + sizeof(SmemCtl) <= kSmemMax, "shared memory layout too large");
 
+template <int N>
+__device__ __forceinline__ void regs_increase()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <int N>
+__device__ __forceinline__ void regs_decrease()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 __device__ __forceinline__ void flag_abort(SmemCtl* c, int* err)
 {
     c->abort = 1;
@@ -262,197 +284,202 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ctl.tmem_base;
-
-    if (warp == kTmaWarp) {
-        // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            tma_prefetch_desc(&tmQ);
-            tma_prefetch_desc(&tmK);
-            tma_prefetch_desc(&tmV);
-            const uint32_t qbar = smem_u32(&ctl.q_full);
-            mbar_arrive_expect_tx(qbar, 2 * kTileBytes);
-            for (int t = 0; t < 2; ++t)
-                for (int h = 0; h < 2; ++h) {
-                    const uint32_t dst = sbase + kSmemQ + t * kTileBytes + h * kBoxBytes;
-                    if (PAGED)
-                        tma_load_3d(dst, &tmQ, qbar, h * 64, w.head[t], w.q_base + w.row0[t]);
-                    else
-                        tma_load_4d(dst, &tmQ, qbar, h * 64, w.head[t], w.row0[t], w.b);
-                }
-            const int* trow = PAGED ? a.block_tables + (size_t)w.b * a.max_blocks : nullptr;
-            // one K or V tile into `dst`: a 64 x 128 box per half (contiguous), or
-            // one 64 x 16 box per half and page (paged; a page past the context, or
-            // any id outside the cache, reads as zeros)
-            auto load_tile = [&](const CUtensorMap* map, uint32_t dst, uint32_t bar, int j) {
-                if (PAGED) {
-                    int phys[kPagesPerTile];
-#pragma unroll
-                    for (int k = 0; k < kPagesPerTile; ++k) {
-                        const int p = j * kPagesPerTile + k;
-                        phys[k] = p < w.n_pages ? trow[p] : -1;
+    // Whole warpgroups re-balance registers, each with one setmaxnreg and then only
+    // its own code: warps 8-11 (MMA, TMA, two idle) down, warps 0-7 (softmax) up.
+    if (warp >= 8) {
+        regs_decrease<kControlRegs>();
+        if (warp == kTmaWarp) {
+            // ------------------------------------------------------------ TMA producer
+            if (lane == 0) {
+                tma_prefetch_desc(&tmQ);
+                tma_prefetch_desc(&tmK);
+                tma_prefetch_desc(&tmV);
+                const uint32_t qbar = smem_u32(&ctl.q_full);
+                mbar_arrive_expect_tx(qbar, 2 * kTileBytes);
+                for (int t = 0; t < 2; ++t)
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t dst = sbase + kSmemQ + t * kTileBytes + h * kBoxBytes;
+                        if (PAGED)
+                            tma_load_3d(dst, &tmQ, qbar, h * 64, w.head[t], w.q_base + w.row0[t]);
+                        else
+                            tma_load_4d(dst, &tmQ, qbar, h * 64, w.head[t], w.row0[t], w.b);
                     }
-#pragma unroll
-                    for (int k = 0; k < kPagesPerTile; ++k)
+                const int* trow = PAGED ? a.block_tables + (size_t)w.b * a.max_blocks : nullptr;
+                // one K or V tile into `dst`: a 64 x 128 box per half (contiguous), or
+                // one 64 x 16 box per half and page (paged; a page past the context, or
+                // any id outside the cache, reads as zeros)
+                auto load_tile = [&](const CUtensorMap* map, uint32_t dst, uint32_t bar, int j) {
+                    if (PAGED) {
+                        int phys[kPagesPerTile];
+    #pragma unroll
+                        for (int k = 0; k < kPagesPerTile; ++k) {
+                            const int p = j * kPagesPerTile + k;
+                            phys[k] = p < w.n_pages ? trow[p] : -1;
+                        }
+    #pragma unroll
+                        for (int k = 0; k < kPagesPerTile; ++k)
+                            for (int h = 0; h < 2; ++h)
+                                tma_load_4d(dst + h * kBoxBytes + k * kPageBoxBytes, map, bar, h * 64, 0,
+                                            w.g, phys[k]);
+                    } else {
                         for (int h = 0; h < 2; ++h)
-                            tma_load_4d(dst + h * kBoxBytes + k * kPageBoxBytes, map, bar, h * 64, 0,
-                                        w.g, phys[k]);
-                } else {
-                    for (int h = 0; h < 2; ++h)
-                        tma_load_4d(dst + h * kBoxBytes, map, bar, h * 64, w.g, j * BN, w.b);
+                            tma_load_4d(dst + h * kBoxBytes, map, bar, h * 64, w.g, j * BN, w.b);
+                    }
+                };
+                int n_k = 0, n_v = 0;  // K / V tiles issued so far
+                bool ok = true;
+                for (int j = 0; j < w.n_kv && ok; ++j) {
+                    const int sk = j % kKStages;
+                    ok = mbar_wait(smem_u32(&ctl.k_empty[sk]), ((j / kKStages) & 1) ^ 1, abort);
+                    if (!ok)
+                        break;
+                    const uint32_t kbar = smem_u32(&ctl.k_full[sk]);
+                    if (j != a.stall_tile) {
+                        mbar_arrive_expect_tx(kbar, kTileBytes);
+                        load_tile(&tmK, sbase + kSmemK + sk * kTileBytes, kbar, j);
+                    }
+                    ++n_k;
+                    const int sv = j % kVStages;
+                    ok = mbar_wait(smem_u32(&ctl.v_empty[sv]), ((j / kVStages) & 1) ^ 1, abort);
+                    if (!ok)
+                        break;
+                    const uint32_t vbar = smem_u32(&ctl.v_full[sv]);
+                    mbar_arrive_expect_tx(vbar, kTileBytes);
+                    load_tile(&tmV, sbase + kSmemV + sv * kTileBytes, vbar, j);
+                    ++n_v;
+                }
+                if (!ok)
+                    flag_abort(&ctl, a.err);
+                // drain: every copy this CTA started has landed before shared memory
+                // is released (bounded by time only, not by the abort flag)
+                const int no_abort = 0;
+                mbar_wait(qbar, 0, &no_abort);
+                for (int s = 0; s < kKStages; ++s) {
+                    // loads issued into stage s: tiles j < n_k with j % kKStages == s,
+                    // except a withheld one
+                    const int c = (n_k > s ? (n_k - s + kKStages - 1) / kKStages : 0) -
+                                  ((a.stall_tile >= 0 && a.stall_tile < n_k && a.stall_tile % kKStages == s) ? 1 : 0);
+                    if (c)
+                        mbar_wait(smem_u32(&ctl.k_full[s]), (c - 1) & 1, &no_abort);
+                }
+                for (int s = 0; s < kVStages; ++s) {
+                    const int c = n_v > s ? (n_v - s + kVStages - 1) / kVStages : 0;
+                    if (c)
+                        mbar_wait(smem_u32(&ctl.v_full[s]), (c - 1) & 1, &no_abort);
+                }
+            }
+        } else if (warp == kMmaWarp) {
+            // ------------------------------------------------------------ MMA warp
+            // The whole warp follows the schedule (so it can clear shared memory
+            // when needed); lane 0 issues the MMAs and commits.
+            const bool leader = lane == 0;
+            const uint32_t idesc_s = idesc_f16_f32(BM, BN, false, false);
+            const uint32_t idesc_o = idesc_f16_f32(BM, D, false, true);
+            // descriptors of the first tile of each region; moving within a region
+            // only adds (byte offset >> 4) to the start-address field (all shared
+            // addresses are below 256 KB, so the 14-bit field cannot overflow)
+            const uint64_t dq = sdesc_sw128(sbase + kSmemQ, 16, 1024);
+            const uint64_t dk = sdesc_sw128(sbase + kSmemK, 16, 1024);
+            const uint64_t dv = sdesc_sw128(sbase + kSmemV, kBoxBytes, 1024);
+            auto issue_s = [&](int t, int s) {
+                const uint64_t aq = dq + ((t * kTileBytes) >> 4);
+                const uint64_t bk = dk + ((s * kTileBytes) >> 4);
+    #pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = ((kk / 4) * kBoxBytes + (kk % 4) * 32) >> 4;
+                    mma_f16_ss(tmem + t * BN, aq + off, bk + off, idesc_s, kk > 0);
                 }
             };
-            int n_k = 0, n_v = 0;  // K / V tiles issued so far
-            bool ok = true;
-            for (int j = 0; j < w.n_kv && ok; ++j) {
-                const int sk = j % kKStages;
-                ok = mbar_wait(smem_u32(&ctl.k_empty[sk]), ((j / kKStages) & 1) ^ 1, abort);
-                if (!ok)
-                    break;
-                const uint32_t kbar = smem_u32(&ctl.k_full[sk]);
-                if (j != a.stall_tile) {
-                    mbar_arrive_expect_tx(kbar, kTileBytes);
-                    load_tile(&tmK, sbase + kSmemK + sk * kTileBytes, kbar, j);
+            auto issue_o = [&](int t, int s, bool acc) {
+                const uint64_t bv = dv + ((s * kTileBytes) >> 4);
+    #pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_f16_ts(tmem + 256 + t * D, tmem + t * BN + kk * 8, bv + ((kk * 2048) >> 4),
+                               idesc_o, (acc || kk > 0) ? 1u : 0u);
+            };
+            auto wait = [&](uint64_t& bar, uint32_t parity) {
+                return __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar), parity, abort));
+            };
+            bool ok = wait(ctl.q_full, 0) && wait(ctl.k_full[0], 0);
+            if (ok) {
+                tc_fence_after();
+                if (leader) {
+                    issue_s(0, 0);
+                    mma_commit(smem_u32(&ctl.s_full[0]));
+                    issue_s(1, 0);
+                    mma_commit(smem_u32(&ctl.s_full[1]));
+                    mma_commit(smem_u32(&ctl.k_empty[0]));
                 }
-                ++n_k;
-                const int sv = j % kVStages;
-                ok = mbar_wait(smem_u32(&ctl.v_empty[sv]), ((j / kVStages) & 1) ^ 1, abort);
-                if (!ok)
-                    break;
-                const uint32_t vbar = smem_u32(&ctl.v_full[sv]);
-                mbar_arrive_expect_tx(vbar, kTileBytes);
-                load_tile(&tmV, sbase + kSmemV + sv * kTileBytes, vbar, j);
-                ++n_v;
-            }
-            if (!ok)
-                flag_abort(&ctl, a.err);
-            // drain: every copy this CTA started has landed before shared memory
-            // is released (bounded by time only, not by the abort flag)
-            const int no_abort = 0;
-            mbar_wait(qbar, 0, &no_abort);
-            for (int s = 0; s < kKStages; ++s) {
-                // loads issued into stage s: tiles j < n_k with j % kKStages == s,
-                // except a withheld one
-                const int c = (n_k > s ? (n_k - s + kKStages - 1) / kKStages : 0) -
-                              ((a.stall_tile >= 0 && a.stall_tile < n_k && a.stall_tile % kKStages == s) ? 1 : 0);
-                if (c)
-                    mbar_wait(smem_u32(&ctl.k_full[s]), (c - 1) & 1, &no_abort);
-            }
-            for (int s = 0; s < kVStages; ++s) {
-                const int c = n_v > s ? (n_v - s + kVStages - 1) / kVStages : 0;
-                if (c)
-                    mbar_wait(smem_u32(&ctl.v_full[s]), (c - 1) & 1, &no_abort);
-            }
-        }
-    } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ MMA warp
-        // The whole warp follows the schedule (so it can clear shared memory
-        // when needed); lane 0 issues the MMAs and commits.
-        const bool leader = lane == 0;
-        const uint32_t idesc_s = idesc_f16_f32(BM, BN, false, false);
-        const uint32_t idesc_o = idesc_f16_f32(BM, D, false, true);
-        // descriptors of the first tile of each region; moving within a region
-        // only adds (byte offset >> 4) to the start-address field (all shared
-        // addresses are below 256 KB, so the 14-bit field cannot overflow)
-        const uint64_t dq = sdesc_sw128(sbase + kSmemQ, 16, 1024);
-        const uint64_t dk = sdesc_sw128(sbase + kSmemK, 16, 1024);
-        const uint64_t dv = sdesc_sw128(sbase + kSmemV, kBoxBytes, 1024);
-        auto issue_s = [&](int t, int s) {
-            const uint64_t aq = dq + ((t * kTileBytes) >> 4);
-            const uint64_t bk = dk + ((s * kTileBytes) >> 4);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = ((kk / 4) * kBoxBytes + (kk % 4) * 32) >> 4;
-                mma_f16_ss(tmem + t * BN, aq + off, bk + off, idesc_s, kk > 0);
-            }
-        };
-        auto issue_o = [&](int t, int s, bool acc) {
-            const uint64_t bv = dv + ((s * kTileBytes) >> 4);
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-                mma_f16_ts(tmem + 256 + t * D, tmem + t * BN + kk * 8, bv + ((kk * 2048) >> 4),
-                           idesc_o, (acc || kk > 0) ? 1u : 0u);
-        };
-        auto wait = [&](uint64_t& bar, uint32_t parity) {
-            return __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar), parity, abort));
-        };
-        bool ok = wait(ctl.q_full, 0) && wait(ctl.k_full[0], 0);
-        if (ok) {
-            tc_fence_after();
-            if (leader) {
-                issue_s(0, 0);
-                mma_commit(smem_u32(&ctl.s_full[0]));
-                issue_s(1, 0);
-                mma_commit(smem_u32(&ctl.s_full[1]));
-                mma_commit(smem_u32(&ctl.k_empty[0]));
-            }
-            __syncwarp();
-        }
-        for (int j = 0; j < w.n_kv && ok; ++j) {
-            const int sv = j % kVStages;
-            const uint32_t phv = (j / kVStages) & 1;
-            const int sk1 = (j + 1) % kKStages;
-            const uint32_t phk1 = ((j + 1) / kKStages) & 1;
-            const bool more = j + 1 < w.n_kv;
-            // Operands first (usually long in place: the warp is idle until tile 0's
-            // P is ready anyway), so that nothing stands between PV0 and S0 below:
-            // each mbarrier wait costs the issuing warp of order a hundred cycles.
-            ok = wait(ctl.v_full[sv], phv) && (!more || wait(ctl.k_full[sk1], phk1)) &&
-                 wait(ctl.p_full[0], j & 1);
-            if (!ok)
-                break;
-            if (PAGED && (j + 1) * BN > w.Lkv) {
-                // Keys from L_kv to the end of the last page are cache slots that may
-                // hold anything (even NaN, and 0 * NaN would reach O through the MMA
-                // although their P is 0): zero those V rows.  Later pages arrive
-                // from TMA as zeros already.
-                const int r0 = w.Lkv - j * BN;
-                const int r1 = min(BN, w.n_pages * kPageSize - j * BN);
-                uint8_t* vt = smem + kSmemV + sv * kTileBytes;
-                for (int idx = lane; idx < (r1 - r0) * 16; idx += 32) {
-                    const int rr = r0 + idx / 16, hh = (idx % 16) / 8, c16 = idx % 8;
-                    *reinterpret_cast<uint4*>(vt + hh * kBoxBytes + rr * 128 + c16 * 16) =
-                        make_uint4(0u, 0u, 0u, 0u);
-                }
-                fence_proxy_async_smem();
                 __syncwarp();
             }
-            tc_fence_after();
-            if (leader) {
-                issue_o(0, sv, j > 0);
-                if (!more)
-                    mma_commit(smem_u32(&ctl.o_full[0]));
-                else {
-                    issue_s(0, sk1);
-                    mma_commit(smem_u32(&ctl.s_full[0]));
+            for (int j = 0; j < w.n_kv && ok; ++j) {
+                const int sv = j % kVStages;
+                const uint32_t phv = (j / kVStages) & 1;
+                const int sk1 = (j + 1) % kKStages;
+                const uint32_t phk1 = ((j + 1) / kKStages) & 1;
+                const bool more = j + 1 < w.n_kv;
+                // Operands first (usually long in place: the warp is idle until tile 0's
+                // P is ready anyway), so that nothing stands between PV0 and S0 below:
+                // each mbarrier wait costs the issuing warp of order a hundred cycles.
+                ok = wait(ctl.v_full[sv], phv) && (!more || wait(ctl.k_full[sk1], phk1)) &&
+                     wait(ctl.p_full[0], j & 1);
+                if (!ok)
+                    break;
+                if (PAGED && (j + 1) * BN > w.Lkv) {
+                    // Keys from L_kv to the end of the last page are cache slots that may
+                    // hold anything (even NaN, and 0 * NaN would reach O through the MMA
+                    // although their P is 0): zero those V rows.  Later pages arrive
+                    // from TMA as zeros already.
+                    const int r0 = w.Lkv - j * BN;
+                    const int r1 = min(BN, w.n_pages * kPageSize - j * BN);
+                    uint8_t* vt = smem + kSmemV + sv * kTileBytes;
+                    for (int idx = lane; idx < (r1 - r0) * 16; idx += 32) {
+                        const int rr = r0 + idx / 16, hh = (idx % 16) / 8, c16 = idx % 8;
+                        *reinterpret_cast<uint4*>(vt + hh * kBoxBytes + rr * 128 + c16 * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
                 }
-            }
-            __syncwarp();
-            ok = wait(ctl.p_full[1], j & 1);
-            if (!ok)
-                break;
-            tc_fence_after();
-            if (leader) {
-                issue_o(1, sv, j > 0);
-                mma_commit(smem_u32(&ctl.v_empty[sv]));
-                if (!more)
-                    mma_commit(smem_u32(&ctl.o_full[1]));
-                if (more) {
-                    issue_s(1, sk1);
-                    mma_commit(smem_u32(&ctl.s_full[1]));
-                    mma_commit(smem_u32(&ctl.k_empty[sk1]));
+                tc_fence_after();
+                if (leader) {
+                    issue_o(0, sv, j > 0);
+                    if (!more)
+                        mma_commit(smem_u32(&ctl.o_full[0]));
+                    else {
+                        issue_s(0, sk1);
+                        mma_commit(smem_u32(&ctl.s_full[0]));
+                    }
                 }
+                __syncwarp();
+                ok = wait(ctl.p_full[1], j & 1);
+                if (!ok)
+                    break;
+                tc_fence_after();
+                if (leader) {
+                    issue_o(1, sv, j > 0);
+                    mma_commit(smem_u32(&ctl.v_empty[sv]));
+                    if (!more)
+                        mma_commit(smem_u32(&ctl.o_full[1]));
+                    if (more) {
+                        issue_s(1, sk1);
+                        mma_commit(smem_u32(&ctl.s_full[1]));
+                        mma_commit(smem_u32(&ctl.k_empty[sk1]));
+                    }
+                }
+                __syncwarp();
             }
-            __syncwarp();
-        }
-        if (leader) {
-            if (!ok)
-                flag_abort(&ctl, a.err);
-            // drain: all MMAs issued by this thread are complete before TMEM is released
-            const int no_abort = 0;
-            mma_commit(smem_u32(&ctl.mma_done));
-            mbar_wait(smem_u32(&ctl.mma_done), 0, &no_abort);
+            if (leader) {
+                if (!ok)
+                    flag_abort(&ctl, a.err);
+                // drain: all MMAs issued by this thread are complete before TMEM is released
+                const int no_abort = 0;
+                mma_commit(smem_u32(&ctl.mma_done));
+                mbar_wait(smem_u32(&ctl.mma_done), 0, &no_abort);
+            }
         }
     } else {
+        regs_increase<kSoftmaxRegs>();
         // ------------------------------------------------------------ softmax warps
         const int t = warp / 4;             // Q tile
         const int quad = warp % 4;          // TMEM lane quadrant = rows [32*quad, +32)
@@ -479,14 +506,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             const bool masked = __any_sync(0xffffffffu, limit < BN);
             uint32_t sr[4][32];
             float rs[8];
-            // Pass over the tile against the current reference max.  On the first
-            // tile (no reference yet) or when this tile's max exceeds the
-            // reference by more than the threshold, it runs a second time after
-            // the reference has moved.
-            bool redo = (j == 0);
-            bool grow = false;
-            float alpha = 1.f;
-            for (int pass = 0; pass < 2; ++pass) {
+            auto load_s = [&]() {
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4)
                     tmem_ld32(tS + q4 * 32, sr[q4]);
@@ -502,31 +522,46 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                             if (q4 * 32 + i >= limit)
                                 sr[q4][i] = __float_as_uint(-CUDART_INF_F);
                 }
-                if (redo) {
-                    // move the reference first (first tile, or the rare fix-up)
-                    const float mx = fmaxf(fmax3(max32(sr[0]), max32(sr[1]), max32(sr[2])), max32(sr[3]));
-                    const float m_new = fmaxf(m_ref, mx * c);
-                    if (m_new > m_ref + kRescaleThreshold) {
-                        grow = true;
-                        alpha = ex2_approx(m_ref - m_new);
-                        m_ref = m_new;
-                        l_sum *= alpha;
-                    }
+            };
+            // move the reference to the tile's row max if it exceeds it by more than
+            // the threshold (always on the first tile, whose reference is -inf)
+            bool grow = false;
+            float alpha = 1.f;
+            auto move_ref = [&](float mx) {
+                const float m_new = fmaxf(m_ref, mx * c);
+                if (m_new > m_ref + kRescaleThreshold) {
+                    grow = true;
+                    alpha = ex2_approx(m_ref - m_new);
+                    m_ref = m_new;
+                    l_sum *= alpha;
                 }
+            };
+            load_s();
+            if (j == 0)
+                move_ref(fmaxf(fmax3(max32(sr[0]), max32(sr[1]), max32(sr[2])), max32(sr[3])));
+            // One straight pass against the current reference, the tile max reduced
+            // alongside (on the first tile the reference is already the max).
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                rs[k] = 0.f;
+            float mx = -CUDART_INF_F;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                mx = fmaxf(mx, max32(sr[q4]));
+                exp_pack32(sr[q4], c, -m_ref, rs);
+            }
+            if (j > 0 && __any_sync(0xffffffffu, mx * c > m_ref + kRescaleThreshold)) {
+                // rare: the reference was too low for this tile.  S is still intact
+                // in TMEM (P has not been written): reload it, move the reference
+                // and redo the pass.
+                move_ref(mx);
+                load_s();
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
                     rs[k] = 0.f;
-                const float neg_m = -m_ref;
-                float mx = -CUDART_INF_F;
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    if (!redo)
-                        mx = fmaxf(mx, max32(sr[q4]));  // reduced alongside the exponentials
-                    exp_pack32(sr[q4], c, neg_m, rs);
-                }
-                if (redo || !__any_sync(0xffffffffu, mx * c > m_ref + kRescaleThreshold))
-                    break;
-                redo = true;  // rare: the optimistic pass used a reference that is too low
+                for (int q4 = 0; q4 < 4; ++q4)
+                    exp_pack32(sr[q4], c, -m_ref, rs);
             }
             // S has been read for the last time: P overwrites its first 64 columns
             tmem_st32_even(tS, sr[0], sr[1]);
@@ -674,6 +709,13 @@ cudaError_t ensure_smem_attr()
         return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(mtx);
     if (!done[dev]) {
+        cudaFuncAttributes fa{};
+        e = cudaFuncGetAttributes(&fa, prefill_kernel<PAGED>);
+        if (e != cudaSuccess)
+            return e;
+        // the warpgroups' register re-balance must fit the pool the CTA launches with
+        if ((long long)fa.numRegs * kThreads < 256LL * kSoftmaxRegs + 128LL * kControlRegs)
+            return cudaErrorInvalidConfiguration;
         e = cudaFuncSetAttribute(prefill_kernel<PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kSmemAlloc);
         if (e != cudaSuccess)
