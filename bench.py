@@ -150,9 +150,17 @@ class ClockSampler:
 # ------------------------------------------------------------------ GPU legs
 
 class Leg:
+    """One hot-path call on one workload.  bind(ins, out) returns a closure that
+    runs it on the given device buffers (ins shaped like dev_in); out_alias is the
+    index of the input that is also the output (in place), else None."""
     def __init__(self, name, kind, work, unit, launches):
         self.name, self.kind, self.work, self.unit, self.launches = name, kind, work, unit, launches
         self.times = []
+        self.out_alias = None
+
+    def set_buffers(self, bind, dev_in, dev_out):
+        self.bind, self.dev_in, self.dev_out = bind, dev_in, dev_out
+        self.run = bind(dev_in, dev_out)
 
     def value(self, ms):
         return self.work / (ms * 1e-3) / (1e12 if self.unit == "TFLOP/s" else 1e9)
@@ -169,8 +177,9 @@ def build_legs(torch, ag, which):
                     if which == "prefill_full" else (W.PREFILL_LONG, W.PREFILL_LONG_FULL)):
             leg = Leg(cfg.name, "prefill", cfg.flops(), "TFLOP/s", 1)
             leg.cfg = cfg
-            leg.run = (lambda c=cfg: ag.attn_prefill(dQ, dK, dV, dO, causal=c.causal))
-            leg.host, leg.dev_in, leg.dev_out = host, (dQ, dK, dV), dO
+            leg.set_buffers(lambda ins, out, c=cfg: (lambda: ag.attn_prefill(*ins, out, causal=c.causal)),
+                            (dQ, dK, dV), dO)
+            leg.host = host
             leg.config = {"B": cfg.B, "S": cfg.S, "H_q": cfg.H_q, "H_kv": cfg.H_kv, "D": cfg.D,
                           "causal": cfg.causal}
             legs.append(leg)
@@ -180,11 +189,10 @@ def build_legs(torch, ag, which):
         t = [torch.from_numpy(x).cuda() for x in (Qp, kc, vc, cu, skv, tables)]
         Op = torch.empty_like(t[0])
         leg = Leg(cfg.name, "prefill", cfg.flops(), "TFLOP/s", 1)
-        leg.run = (lambda t=t, Op=Op, c=cfg: ag.attn_prefill_paged(
-            t[0], t[1], t[2], Op, t[3], t[4], t[5], c.chunk, causal=c.causal))
+        leg.set_buffers(lambda t, o, c=cfg: (lambda: ag.attn_prefill_paged(
+            t[0], t[1], t[2], o, t[3], t[4], t[5], c.chunk, causal=c.causal)), tuple(t), Op)
         leg.host = {"Q": Qp, "k_cache": kc, "v_cache": vc, "cu_seqlens_q": cu, "seq_lens_kv": skv,
                     "block_tables": tables}
-        leg.dev_in, leg.dev_out = tuple(t), Op
         leg.config = {"num_seqs": cfg.num_seqs, "prefix": cfg.prefix, "chunk": cfg.chunk,
                       "H_q": cfg.H_q, "H_kv": cfg.H_kv, "D": cfg.D, "causal": cfg.causal,
                       "block_size": 16, "num_blocks": int(kc.shape[0])}
@@ -197,10 +205,10 @@ def build_legs(torch, ag, which):
                                                   inp.block_tables, inp.seq_lens)]
         out = torch.empty_like(t[0])
         leg = Leg(cfg.name, "decode", float(inp.kv_bytes()), "GB/s", 2)
-        leg.run = (lambda t=t, out=out: ag.attn_decode_paged(t[0], t[1], t[2], out, t[3], t[4]))
+        leg.set_buffers(lambda t, o: (lambda: ag.attn_decode_paged(t[0], t[1], t[2], o, t[3], t[4])),
+                        tuple(t), out)
         leg.host = {"q": inp.q, "k_cache": inp.k_cache, "v_cache": inp.v_cache,
                     "block_tables": inp.block_tables, "seq_lens": inp.seq_lens}
-        leg.dev_in, leg.dev_out = tuple(t), out
         leg.config = {"num_seqs": cfg.num_seqs, "H_q": cfg.H_q, "H_kv": cfg.H_kv, "D": cfg.D,
                       "block_size": cfg.block_size, "seq_len": [cfg.len_lo, cfg.len_hi],
                       "max_blocks_per_seq": cfg.max_blocks_per_seq,
@@ -218,10 +226,9 @@ def build_legs(torch, ag, which):
             dkn, dvn, dsl = (torch.from_numpy(x).cuda() for x in (kn, vn, slots))
             app_bytes = 2 * kn.nbytes
             leg2 = Leg(cfg.name + "_append", "decode", float(inp.kv_bytes() + app_bytes), "GB/s", 3)
-            leg2.run = (lambda t=t, out=out, dkn=dkn, dvn=dvn, dsl=dsl: ag.attn_decode_paged_append(
-                t[0], dkn, dvn, t[1], t[2], out, dsl, t[3], t[4]))
+            leg2.set_buffers(lambda t, o: (lambda: ag.attn_decode_paged_append(
+                t[0], t[5], t[6], t[1], t[2], o, t[7], t[3], t[4])), tuple(t) + (dkn, dvn, dsl), out)
             leg2.host = dict(leg.host, k_new=kn, v_new=vn, slot_mapping=slots)
-            leg2.dev_in, leg2.dev_out = tuple(t) + (dkn, dvn, dsl), out
             leg2.config = dict(leg.config, append_bytes=app_bytes)
             legs.append(leg2)
     if which in ("all", "prologue"):
@@ -238,11 +245,11 @@ def build_legs(torch, ag, which):
         cs = torch.empty((cfg.seq_len, cfg.D), dtype=torch.float32, device="cuda")
         ag.attn_rope_cos_sin_table(cs, cfg.base)
         leg = Leg(cfg.name, "prologue", cfg.bytes(), "GB/s", 1)
-        leg.run = (lambda t=t, kc=kc, vc=vc, cs=cs: ag.attn_qk_norm_rope_append(
-            t[0], t[1], t[2], t[3], t[4], cs, t[5], t[6], kc, vc, eps=1e-6))
+        leg.set_buffers(lambda t, o, kc=kc, vc=vc, cs=cs: (lambda: ag.attn_qk_norm_rope_append(
+            t[0], t[1], t[2], t[3], t[4], cs, t[5], t[6], kc, vc, eps=1e-6)), tuple(t), t[0])
+        leg.out_alias = 0   # q is rotated in place: the step's result is its q
         leg.host = {"Q": Q, "K": K, "V": V, "q_weight": qw, "k_weight": kw, "positions": pos,
                     "slot_mapping": slots}
-        leg.dev_in, leg.dev_out = tuple(t), t[0]
         leg.config = {"tokens": cfg.tokens, "seq_len": cfg.seq_len, "H_q": cfg.H_q,
                       "H_kv": cfg.H_kv, "D": cfg.D, "rope_base": cfg.base, "eps": 1e-6,
                       "block_size": 16, "num_blocks": nb, "bytes": cfg.bytes()}
@@ -277,32 +284,60 @@ def time_device(torch, legs, steps, warmup, dist, use_cuda):
 
 
 def time_e2e(torch, leg, steps, warmup):
-    """Same leg through the public API with pinned host buffers: H2D of the
-    inputs, the C-ABI call, D2H of the output, all inside the timed region."""
+    """Same leg through the public API with pinned host buffers: every step copies
+    its inputs host-to-device, makes the C-ABI call and copies its result back, all
+    inside the timed region.  Steps are pipelined the way a serving loop would run
+    them: two device buffer sets and three streams (copies in, kernels, copies out),
+    so the copies of one step overlap the kernels of its neighbours; events keep a
+    buffer set from being refilled before its previous step's kernels and result
+    copy are done."""
     pinned_in = [torch.from_numpy(np.ascontiguousarray(x)).pin_memory() for x in leg.host.values()]
-    pinned_out = torch.empty(leg.dev_out.shape, dtype=leg.dev_out.dtype).pin_memory()
-    stream = torch.cuda.current_stream()
+    pinned_out = [torch.empty(leg.dev_out.shape, dtype=leg.dev_out.dtype).pin_memory() for _ in range(2)]
+    second_in = tuple(torch.empty_like(x) for x in leg.dev_in)
+    second_out = second_in[leg.out_alias] if leg.out_alias is not None else torch.empty_like(leg.dev_out)
+    sets = [(leg.dev_in, leg.dev_out), (second_in, second_out)]
+    runs = [leg.bind(ins, out) for ins, out in sets]
+    s_in, s_run, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_run = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    def step():
-        for h, d in zip(pinned_in, leg.dev_in):
-            d.copy_(h, non_blocking=True)
-        leg.run()
-        pinned_out.copy_(leg.dev_out, non_blocking=True)
+    def step(i):
+        b = i % 2
+        ins, out = sets[b]
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(ev_run[b])      # its previous kernels have read the inputs
+            for h, d in zip(pinned_in, ins):
+                d.copy_(h, non_blocking=True)
+            ev_in[b].record(s_in)
+        with torch.cuda.stream(s_run):
+            s_run.wait_event(ev_in[b])
+            if i >= 2:
+                s_run.wait_event(ev_out[b])     # its previous result has been copied out
+            runs[b]()
+            ev_run[b].record(s_run)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_run[b])
+            pinned_out[b].copy_(out, non_blocking=True)
+            ev_out[b].record(s_out)
 
-    for _ in range(warmup):
-        step()
+    for i in range(warmup):
+        step(i)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(steps):
-        step()
-    b.record(stream)
+    a.record(s_in)
+    for i in range(steps):
+        step(i)
+    s_in.wait_event(ev_out[(steps - 1) % 2])
+    b.record(s_in)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
     bi = sum(x.numel() * x.element_size() for x in pinned_in)
-    bo = pinned_out.numel() * pinned_out.element_size()
+    bo = pinned_out[0].numel() * pinned_out[0].element_size()
     return {"value": leg.value(ms), "unit": leg.unit, "ms": ms,
-            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+            "pipeline": "2 buffer sets, 3 streams (copy in / kernels / copy out)"}
 
 
 # ------------------------------------------------------------------ CPU oracle
