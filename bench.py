@@ -183,6 +183,21 @@ def build_legs(torch, ag, which):
             leg.config = {"B": cfg.B, "S": cfg.S, "H_q": cfg.H_q, "H_kv": cfg.H_kv, "D": cfg.D,
                           "causal": cfg.causal}
             legs.append(leg)
+    if which == "qwen":
+        # the Qwen3-0.6B attention shape (B=4, S=1024, H 16/8, causal): 50 MB of inputs and
+        # outputs fit in L2, so it is timed twice, as is and with L2 flushed before each launch
+        cfg = W.PREFILL_QWEN
+        Q, K, V = W.prefill_inputs(cfg, seed=0)
+        dQ, dK, dV = (torch.from_numpy(x).cuda() for x in (Q, K, V))
+        dO = torch.empty_like(dQ)
+        for flush in (False, True):
+            leg = Leg(cfg.name + ("_l2flush" if flush else ""), "prefill", cfg.flops(), "TFLOP/s", 1)
+            leg.set_buffers(lambda ins, out: (lambda: ag.attn_prefill(*ins, out, causal=True)), (dQ, dK, dV), dO)
+            leg.host = {"Q": Q, "K": K, "V": V}
+            leg.flush = flush
+            leg.config = {"B": cfg.B, "S": cfg.S, "H_q": cfg.H_q, "H_kv": cfg.H_kv, "D": cfg.D,
+                          "causal": True, "l2": "flushed before each launch" if flush else "warm"}
+            legs.append(leg)
     if which in ("all", "prefill_paged"):
         cfg = W.CHUNKED_PREFILL
         Qp, kc, vc, cu, skv, tables = W.chunked_prefill_inputs(cfg, seed=0)
@@ -259,6 +274,10 @@ def build_legs(torch, ag, which):
 
 def time_device(torch, legs, steps, warmup, dist, use_cuda):
     stream = torch.cuda.current_stream()
+    # a buffer larger than L2 (129 MB), rewritten outside the timed events of legs
+    # that ask for a cold L2
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device="cuda") \
+        if any(getattr(leg, "flush", False) for leg in legs) else None
     for _ in range(warmup):
         for leg in legs:
             leg.run()
@@ -271,6 +290,8 @@ def time_device(torch, legs, steps, warmup, dist, use_cuda):
     t0 = time.perf_counter()
     for s in range(steps):
         for i, leg in enumerate(legs):
+            if getattr(leg, "flush", False):
+                flush_buf.fill_(s & 0xff)
             ev[s][i][0].record(stream)
             leg.run()
             ev[s][i][1].record(stream)
@@ -341,6 +362,26 @@ def time_e2e(torch, leg, steps, warmup):
 
 
 # ------------------------------------------------------------------ CPU oracle
+
+def cpu_model() -> str:
+    try:   # lscpu names Arm cores too (/proc/cpuinfo on Arm has no model name)
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
 
 def oracle_sample(seconds: float, seed: int = 0):
     """Time the FP64 oracle on random rows of the causal prefill workload until
@@ -430,6 +471,7 @@ def run_ours(args):
     if rank == 0 and not args.no_cpu_baseline:
         tf, n, secs, threads = oracle_sample(args.cpu_seconds)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "cpu": cpu_model(), "nproc": os.cpu_count(),
                "sample": f"{n} random rows (b,i,h) of {W.PREFILL_LONG.name}, FP64, {secs:.1f} s"}
 
     head = parts[0]
@@ -477,7 +519,7 @@ def run_reference(args):
         "config": {"workload": W.PREFILL_LONG.name, "B": 2, "S": 8192, "H_q": 32, "H_kv": 8,
                    "D": 128, "causal": True},
         "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                         "sample": sample},
+                         "cpu": cpu_model(), "nproc": os.cpu_count(), "sample": sample},
         "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -489,7 +531,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["all", "prefill", "prefill_full", "prefill_paged", "prologue", "decode",
+    ap.add_argument("--workload", choices=["all", "prefill", "prefill_full", "prefill_paged", "prologue", "qwen", "decode",
                                            "decode_long", "decode_append"],
                     default="all")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
