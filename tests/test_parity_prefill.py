@@ -127,3 +127,15 @@ def test_unsupported_head_dim_raises():
     with pytest.raises(ag.AttnError) as e:
         ag.attn_prefill(Q, Q[:, :, :1].contiguous(), Q[:, :, :1].contiguous(), Q.clone())
     assert e.value.status == ag.ATTN_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("heads", [(32, 2), (15, 3), (48, 4), (64, 64)])
+def test_wide_groups_and_many_heads(causal, heads):
+    # group 16 and 12 (head pairs), group 5 (odd: row pairs), and 64-head MHA
+    H_q, H_kv = heads
+    S = 333
+    Q, K, V = rand_inputs(1, S, H_q, H_kv, seed=H_q * 31 + H_kv)
+    assert_close(run_prefill(Q, K, V, causal), oracle.prefill(Q, K, V, causal=causal),
+                 f"S={S} causal={causal} heads={heads}")
+    assert device_error_clean()

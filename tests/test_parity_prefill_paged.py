@@ -101,3 +101,15 @@ def test_device_length_checks():
     assert ag.attn_get_device_error(reset=True) & 64
     ref = oracle.prefill_paged(Q, kc, vc, cu, skv, table)
     assert_close(out[:10 + 128], ref[:10 + 128], "rows within max_seqlen_q")
+
+
+@pytest.mark.parametrize("heads", [(32, 2), (5, 1), (64, 64)])
+def test_wide_groups_and_many_heads(heads):
+    H_q, H_kv = heads
+    rng = np.random.default_rng(65 + H_q)
+    lens_q, prefix = [150, 1, 300], [200, 63, 0]
+    _, _, kc, vc, table, Q, cu, skv = _paged_problem(rng, [q + p for q, p in zip(lens_q, prefix)],
+                                                     lens_q, H_q, H_kv, 128)
+    out = run(Q, kc, vc, cu, skv, table)
+    assert_close(out, oracle.prefill_paged(Q, kc, vc, cu, skv, table), f"paged prefill heads={heads}")
+    assert device_error_clean()

@@ -241,3 +241,21 @@ def test_bench_workload_sampled():
     gv = host(vc)[s // 16, :, s % 16, :]
     assert_rounded(gk, oracle.qk_norm_rope(K[pick], kw, pos[pick], cfg.base, EPS), "K sample")
     assert np.array_equal(gv.view(np.uint16), V[pick].view(np.uint16))
+
+
+def test_append_at_the_row_limit():
+    # H_q + 2 * H_kv = 192 rows per token: the most one token may stage
+    rng = np.random.default_rng(88)
+    T, H_q, H_kv, nb, max_pos = 37, 96, 48, 4, 500
+    Q, K, V, qw, kw, pos, slots = _append_case(rng, T, H_q, H_kv, nb, max_pos)
+    kc = torch.zeros((nb, H_kv, 16, 128), dtype=torch.float16, device="cuda")
+    vc = torch.zeros_like(kc)
+    dQ = dev(Q)
+    ag.attn_qk_norm_rope_append(dQ, dev(K), dev(V), dev(qw), dev(kw), table(max_pos), dev(pos),
+                                dev(slots), kc, vc, eps=EPS)
+    torch.cuda.synchronize()
+    assert device_error_clean()
+    assert_rounded(host(dQ), oracle.qk_norm_rope(Q, qw, pos, BASE, EPS), "Q at the row limit")
+    gk, gv = host(kc), host(vc)
+    assert_rounded(gk[slots // 16, :, slots % 16, :], oracle.qk_norm_rope(K, kw, pos, BASE, EPS), "K")
+    assert np.array_equal(gv[slots // 16, :, slots % 16, :].view(np.uint16), V.view(np.uint16))
