@@ -16,11 +16,14 @@
 // packed query chunks whose first query sits after a cached prefix
 // (L_kv - L_q keys): query i of a sequence attends to keys <= L_kv - L_q + i.
 //
-// GB300 design (one CTA per SM, 320 threads):
+// GB300 design (one CTA per SM, 384 threads = three warpgroups):
 //   warps 0-3  softmax of Q tile 0 (TMEM lanes 0..127 = its rows)
 //   warps 4-7  softmax of Q tile 1
 //   warp  8    MMA warp (one lane issues) + TMEM allocation
 //   warp  9    TMA producer (one lane)
+//   warps 10-11 idle (they complete the third warpgroup)
+// After setup the warpgroups re-balance registers with setmaxnreg: the two
+// softmax warpgroups rise to 200 per thread, the MMA/TMA warpgroup drops to 96.
 // A CTA owns two 128-row Q tiles that read the same K/V: two query heads of
 // one GQA group over the same rows when the group size is even (identical
 // causal extents), else two consecutive row tiles of one head.  Per 128-key
