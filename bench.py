@@ -408,11 +408,12 @@ def cpu_model() -> str:
     return platform.processor() or platform.machine()
 
 
-def oracle_sample(seconds: float, seed: int = 0):
-    """Time the FP64 oracle on random rows of the causal prefill workload until
-    about `seconds` of CPU time; returns (TFLOP/s, rows, wall seconds, threads)."""
+def oracle_sample(seconds: float, seed: int = 0, cfg=None):
+    """Time the FP64 oracle on random rows of a causal prefill workload (the
+    long one by default) until about `seconds` of CPU time; returns (TFLOP/s,
+    rows, wall seconds, threads)."""
     import oracle
-    cfg = W.PREFILL_LONG
+    cfg = cfg or W.PREFILL_LONG
     Q, K, V = W.prefill_inputs(cfg, seed=0)
     rng = np.random.default_rng(seed)
     threads = oracle.num_threads()
@@ -440,6 +441,40 @@ def oracle_sample(seconds: float, seed: int = 0):
         total_t += dt
         total_n += n
     return total_f / total_t / 1e12, total_n, total_t, threads
+
+
+def oracle_decode_sample(seconds: float, seed: int = 0, n_seqs: int = 16):
+    """Time the FP64 oracle on the decode mix: `n_seqs` sequences drawn with
+    the workload's length distribution, every query head of each, repeated
+    until about `seconds`; returns (GB/s of valid K/V bytes, sequences, wall
+    seconds, threads)."""
+    import oracle
+    cfg = W.DECODE_MIX
+    small = W.DecodeConfig(cfg.name, n_seqs, cfg.H_q, cfg.H_kv, cfg.D, cfg.block_size,
+                           cfg.len_lo, cfg.len_hi, cfg.max_blocks_per_seq)
+    d = W.decode_inputs(small, seed=seed)
+    total_b, total_t, total_n = 0.0, 0.0, 0
+    while total_t < seconds:
+        t = time.perf_counter()
+        oracle.decode_paged(d.q, d.k_cache, d.v_cache, d.block_tables, d.seq_lens)
+        total_t += time.perf_counter() - t
+        total_b += d.kv_bytes()
+        total_n += n_seqs
+    return total_b / total_t / 1e9, total_n, total_t, oracle.num_threads()
+
+
+def cpu_baseline_extras(seconds: float):
+    """Two further oracle figures: the Qwen3-0.6B-shaped prefill on one core,
+    and the decode mix on every core (GB/s of K/V)."""
+    import oracle
+    with oracle.threads(1):
+        tf, n, secs, _ = oracle_sample(seconds, cfg=W.PREFILL_QWEN)
+    one = {"workload": W.PREFILL_QWEN.name, "value": tf, "unit": "TFLOP/s", "cores": 1,
+           "sample": f"{n} random rows (b,i,h), FP64, {secs:.1f} s"}
+    gbs, n, secs, threads = oracle_decode_sample(seconds)
+    dec = {"workload": W.DECODE_MIX.name, "value": gbs, "unit": "GB/s", "cores": threads,
+           "sample": f"{n} sequences drawn with the workload's lengths, all heads, FP64, {secs:.1f} s"}
+    return [one, dec]
 
 
 # ------------------------------------------------------------------ arms
@@ -497,7 +532,8 @@ def run_ours(args):
         tf, n, secs, threads = oracle_sample(args.cpu_seconds)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "cpu": cpu_model(), "nproc": os.cpu_count(),
-               "sample": f"{n} random rows (b,i,h) of {W.PREFILL_LONG.name}, FP64, {secs:.1f} s"}
+               "sample": f"{n} random rows (b,i,h) of {W.PREFILL_LONG.name}, FP64, {secs:.1f} s",
+               "also": cpu_baseline_extras(max(1.0, args.cpu_seconds / 5))}
 
     head = parts[0]
     launches = sum(leg.launches for leg in legs) * args.steps

@@ -49,6 +49,8 @@ def _bind(lib):
     lib.oracle_half_to_double.restype = ctypes.c_double
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = i
+    lib.oracle_set_num_threads.argtypes = [i]
+    lib.oracle_set_num_threads.restype = None
     lib.oracle_prefill.argtypes = [p, p, p, i, i, i, i, i, i, p, p]
     lib.oracle_prefill.restype = None
     lib.oracle_prefill_rows.argtypes = [p, p, p, i, i, i, i, i, i, p, i, p, p]
@@ -91,6 +93,18 @@ def _i32(a) -> np.ndarray:
 def num_threads() -> int:
     """OpenMP threads the oracle uses (OMP_NUM_THREADS, else all cores)."""
     return int(_load().oracle_num_threads())
+
+
+@contextlib.contextmanager
+def threads(n: int):
+    """Run the oracle's calls inside the block on ``n`` OpenMP threads."""
+    lib = _load()
+    saved = int(lib.oracle_num_threads())
+    lib.oracle_set_num_threads(int(n))
+    try:
+        yield
+    finally:
+        lib.oracle_set_num_threads(saved)
 
 
 def half_to_double(bits: int) -> float:

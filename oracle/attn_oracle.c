@@ -79,6 +79,17 @@ int oracle_num_threads(void)
 #endif
 }
 
+/* Threads for the calls that follow (n >= 1); used to time the oracle on one core. */
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n >= 1)
+        omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /*
  * Attention of one query vector over n keys.
  * q: D halves.  key(j) / val(j): pointers to the j-th key / value row (D halves).

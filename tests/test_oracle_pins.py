@@ -170,6 +170,20 @@ def test_prefill_rows_equal_full():
             assert np.array_equal(Or[r], O[b, i, h]) and lr[r] == lse[b, i, h]
 
 
+def test_thread_count_does_not_change_results():
+    # every output row is one independent loop: one thread or many, same bits
+    B, S, H_q, H_kv, D = 1, 24, 4, 2, 16
+    rng = np.random.default_rng(17)
+    Q, K, V = _rand16(rng, (B, S, H_q, D)), _rand16(rng, (B, S, H_kv, D)), _rand16(rng, (B, S, H_kv, D))
+    O, lse = oracle.prefill(Q, K, V, with_lse=True)
+    before = oracle.num_threads()
+    with oracle.threads(1):
+        assert oracle.num_threads() == 1
+        O1, lse1 = oracle.prefill(Q, K, V, with_lse=True)
+    assert oracle.num_threads() == before
+    assert np.array_equal(O, O1) and np.array_equal(lse, lse1)
+
+
 # ------------------------------------------------------------------ decode
 
 def _page(K, bs, perm):
