@@ -107,6 +107,7 @@ struct PrefillArgs {
     const int* seq_lens_kv;   // [B] context lengths (prefix + chunk)
     const int* block_tables;  // [B, max_blocks]
     int max_blocks;
+    int total_q;              // rows of packed Q / O
 };
 
 struct Unit {
@@ -145,8 +146,14 @@ __device__ __forceinline__ Unit decode_unit(const PrefillArgs& a, int u)
         w.q_base = w.b * a.S;
         w.Lq = w.Lkv = a.S;
     } else {
-        w.q_base = a.cu_q[w.b];
-        w.Lq = a.cu_q[w.b + 1] - w.q_base;
+        const int c0 = a.cu_q[w.b], c1 = a.cu_q[w.b + 1];
+        // a chunk whose rows are not inside packed Q / O is flagged and becomes
+        // empty (skipped below)
+        const bool rows_ok = c0 >= 0 && c1 >= c0 && c1 <= a.total_q;
+        w.q_base = rows_ok ? c0 : 0;
+        w.Lq = rows_ok ? c1 - c0 : 0;
+        if (!rows_ok)
+            w.flags |= kDevErrBadLengths;
         w.Lkv = a.seq_lens_kv[w.b];
         const int max_len = a.max_blocks * kPageSize;
         if (w.Lkv > max_len) {
@@ -176,6 +183,7 @@ struct SmemCtl {
     uint64_t v_full[kVStages], v_empty[kVStages];
     uint64_t s_full[2], p_full[2], o_full[2];
     uint64_t mma_done;
+    uint64_t epi_ready[2];   // a tile's O rows are in shared memory (128 arrivals)
     uint32_t tmem_base;
     int abort;
 };
@@ -238,7 +246,8 @@ __device__ __forceinline__ void exp_pack32(uint32_t (&r)[32], float c, float neg
 template <bool PAGED>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-               const __grid_constant__ CUtensorMap tmV, const PrefillArgs a)
+               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+               const PrefillArgs a)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -275,6 +284,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             mbar_init(smem_u32(&ctl.s_full[t]), 1);
             mbar_init(smem_u32(&ctl.p_full[t]), 128);
             mbar_init(smem_u32(&ctl.o_full[t]), 1);
+            mbar_init(smem_u32(&ctl.epi_ready[t]), 128);
         }
         mbar_init(smem_u32(&ctl.mma_done), 1);
         fence_mbar_init();
@@ -297,6 +307,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 tma_prefetch_desc(&tmQ);
                 tma_prefetch_desc(&tmK);
                 tma_prefetch_desc(&tmV);
+                tma_prefetch_desc(&tmO);
                 const uint32_t qbar = smem_u32(&ctl.q_full);
                 mbar_arrive_expect_tx(qbar, 2 * kTileBytes);
                 for (int t = 0; t < 2; ++t)
@@ -600,24 +611,55 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         } else {
             tc_fence_after();
             const float inv = 1.f / l_sum;
+            // A whole tile leaves through shared memory and two TMA stores: Q_t's
+            // buffer is free (every S GEMM that read it completed before o_full),
+            // each thread writes its row there in the 128-byte swizzled layout of
+            // the O tensor map's boxes (conflict-free: 8 consecutive rows cover all
+            // 16-byte bank groups), and one thread stores the tile.  A tile that
+            // runs past the end of the sequence (chunk) stores its rows one by one.
+            const bool whole = my_row0 + BM <= w.Lq;   // uniform over the warpgroup
             const bool store = q_row < w.Lq;
             __half* dst = a.O + ((size_t)(w.q_base + q_row) * a.H_q + my_head) * D;
+            uint8_t* const stile = smem + kSmemQ + t * kTileBytes;
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
                 uint32_t orr[32];
                 tmem_ld32(tO + q4 * 32, orr);
                 tmem_ld_wait();
                 reg_fence32(orr);
-                if (store) {
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        uint4 pk;
-                        pk.x = pack_half2(__uint_as_float(orr[8 * v + 0]) * inv, __uint_as_float(orr[8 * v + 1]) * inv);
-                        pk.y = pack_half2(__uint_as_float(orr[8 * v + 2]) * inv, __uint_as_float(orr[8 * v + 3]) * inv);
-                        pk.z = pack_half2(__uint_as_float(orr[8 * v + 4]) * inv, __uint_as_float(orr[8 * v + 5]) * inv);
-                        pk.w = pack_half2(__uint_as_float(orr[8 * v + 6]) * inv, __uint_as_float(orr[8 * v + 7]) * inv);
+                for (int v = 0; v < 4; ++v) {
+                    uint4 pk;
+                    pk.x = pack_half2(__uint_as_float(orr[8 * v + 0]) * inv, __uint_as_float(orr[8 * v + 1]) * inv);
+                    pk.y = pack_half2(__uint_as_float(orr[8 * v + 2]) * inv, __uint_as_float(orr[8 * v + 3]) * inv);
+                    pk.z = pack_half2(__uint_as_float(orr[8 * v + 4]) * inv, __uint_as_float(orr[8 * v + 5]) * inv);
+                    pk.w = pack_half2(__uint_as_float(orr[8 * v + 6]) * inv, __uint_as_float(orr[8 * v + 7]) * inv);
+                    if (whole) {
+                        const int c16 = q4 * 4 + v;   // 16-byte chunk of the 256-byte row
+                        *reinterpret_cast<uint4*>(stile + (c16 / 8) * kBoxBytes + row * 128 +
+                                                  (((c16 % 8) ^ (row % 8)) << 4)) = pk;
+                    } else if (store) {
                         *reinterpret_cast<uint4*>(dst + q4 * 32 + v * 8) = pk;
                     }
+                }
+            }
+            if (whole) {
+                // the storing thread waits (bounded) for all 128 rows; a warp that
+                // left on an abort never arrives, and then nothing is stored
+                fence_proxy_async_smem();
+                mbar_arrive(smem_u32(&ctl.epi_ready[t]));
+                if (quad == 0 && lane == 0 && mbar_wait(smem_u32(&ctl.epi_ready[t]), 0, abort)) {
+                    const uint32_t src = sbase + kSmemQ + t * kTileBytes;
+                    for (int h = 0; h < 2; ++h) {
+                        if (PAGED)
+                            tma_store_3d(&tmO, src + h * kBoxBytes, h * 64, my_head, w.q_base + my_row0);
+                        else
+                            tma_store_4d(&tmO, src + h * kBoxBytes, h * 64, my_head, my_row0, w.b);
+                    }
+                    bulk_commit_group();
+                    bulk_wait_group_read0();   // shared memory stays valid until read
+                } else if (quad == 0 && lane == 0) {
+                    flag_abort(&ctl, a.err);
                 }
             }
         }
@@ -751,9 +793,9 @@ cudaError_t launch_prefill(const void* Q, const void* K, const void* V, void* O,
     cudaError_t e = ensure_smem_attr<false>();
     if (e != cudaSuccess)
         return e;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     if (!make_bshd_map(&mq, Q, B, S, H_q) || !make_bshd_map(&mk, K, B, S, H_kv) ||
-        !make_bshd_map(&mv, V, B, S, H_kv))
+        !make_bshd_map(&mv, V, B, S, H_kv) || !make_bshd_map(&mo, O, B, S, H_q))
         return cudaErrorInvalidValue;
     PrefillArgs a{};
     a.O = static_cast<__half*>(O);
@@ -766,7 +808,7 @@ cudaError_t launch_prefill(const void* Q, const void* K, const void* V, void* O,
     const long long grid = (long long)a.units_per_mb * a.n_mb;
     if (grid > 0x7fffffffLL)
         return cudaErrorInvalidConfiguration;
-    prefill_kernel<false><<<(unsigned)grid, kThreads, kSmemAlloc, stream>>>(mq, mk, mv, a);
+    prefill_kernel<false><<<(unsigned)grid, kThreads, kSmemAlloc, stream>>>(mq, mk, mv, mo, a);
     return cudaGetLastError();
 }
 
@@ -779,9 +821,9 @@ cudaError_t launch_prefill_paged(const void* Q, const void* k_cache, const void*
     cudaError_t e = ensure_smem_attr<true>();
     if (e != cudaSuccess)
         return e;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     if (!make_packed_map(&mq, Q, total_q, H_q) || !make_cache_map(&mk, k_cache, num_blocks, H_kv) ||
-        !make_cache_map(&mv, v_cache, num_blocks, H_kv))
+        !make_cache_map(&mv, v_cache, num_blocks, H_kv) || !make_packed_map(&mo, O, total_q, H_q))
         return cudaErrorInvalidValue;
     PrefillArgs a{};
     a.O = static_cast<__half*>(O);
@@ -794,10 +836,11 @@ cudaError_t launch_prefill_paged(const void* Q, const void* k_cache, const void*
     a.seq_lens_kv = seq_lens_kv;
     a.block_tables = block_tables;
     a.max_blocks = max_blocks_per_seq;
+    a.total_q = total_q;
     const long long grid = (long long)a.units_per_mb * a.n_mb;
     if (grid > 0x7fffffffLL)
         return cudaErrorInvalidConfiguration;
-    prefill_kernel<true><<<(unsigned)grid, kThreads, kSmemAlloc, stream>>>(mq, mk, mv, a);
+    prefill_kernel<true><<<(unsigned)grid, kThreads, kSmemAlloc, stream>>>(mq, mk, mv, mo, a);
     return cudaGetLastError();
 }
 

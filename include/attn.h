@@ -76,9 +76,10 @@ ATTN_API int attn_prefill(const void* Q, const void* K, const void* V, void* O, 
  * D must be 128 and block_size 16.  B, total_q or max_seqlen_q == 0 is a no-op.
  * Cache slots past a context and table entries past its pages may hold
  * anything; a page id outside [0, num_blocks) reads as zeros.  Device-checked
- * preconditions (flagged, ATTN_ERR_BAD_INPUT): L_q <= L_kv (else the
- * sequence is skipped), L_q <= max_seqlen_q (else its extra rows are not
- * computed), L_kv <= max_blocks_per_seq*block_size (else clamped).
+ * preconditions (flagged, ATTN_ERR_BAD_INPUT): 0 <= cu_seqlens_q[b] <=
+ * cu_seqlens_q[b+1] <= total_q and L_q <= L_kv (else the sequence is skipped),
+ * L_q <= max_seqlen_q (else its extra rows are not computed), L_kv <=
+ * max_blocks_per_seq*block_size (else clamped).
  */
 ATTN_API int attn_prefill_paged(const void* Q, const void* k_cache, const void* v_cache, void* O,
                                 const int* cu_seqlens_q, const int* seq_lens_kv,

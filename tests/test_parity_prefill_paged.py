@@ -103,6 +103,23 @@ def test_device_length_checks():
     assert_close(out[:10 + 128], ref[:10 + 128], "rows within max_seqlen_q")
 
 
+def test_chunk_offsets_outside_packed_rows_are_skipped():
+    rng = np.random.default_rng(66)
+    _, _, kc, vc, table, Q, cu, skv = _paged_problem(rng, [300, 400], [200, 150], 4, 2, 128)
+    bad = cu.copy()
+    bad[2] = cu[2] + 40                          # the second chunk would run past packed Q / O
+    out = run(Q, kc, vc, bad, skv, table, max_q=200)
+    assert ag.attn_get_device_error(reset=True) & 64
+    ref = oracle.prefill_paged(Q[:200], kc, vc, cu[:2], skv[:1], table[:1])
+    assert_close(out[:200], ref, "good sequence next to one outside packed Q")
+    assert np.isnan(out[200:].astype(np.float32)).all()
+    bad = cu.copy()
+    bad[1] = -8                                  # negative offset: both chunks are skipped
+    out = run(Q, kc, vc, bad, skv, table, max_q=200)
+    assert ag.attn_get_device_error(reset=True) & 64
+    assert np.isnan(out.astype(np.float32)).all()
+
+
 @pytest.mark.parametrize("heads", [(32, 2), (5, 1), (64, 64)])
 def test_wide_groups_and_many_heads(heads):
     H_q, H_kv = heads
