@@ -42,7 +42,7 @@
 // rescales O and recomputes.  This keeps the max reduction off the path from
 // "S ready" to "P ready" that the tensor core waits for.
 // TMEM: S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512) columns.
-// SMEM: Q0,Q1 (32 KB each), 2 K stages, 3 V stages (32 KB each), all
+// SMEM: Q0,Q1 (32 KB each), 2 K stages, 2 V stages (32 KB each), all
 // 128-byte swizzled as written by TMA boxes of 64 x 128 (contiguous K/V) or
 // 64 x 16 (one cache page).  Key tiles wholly above the diagonal are never
 // loaded or multiplied; only the diagonal tile is masked.
@@ -79,7 +79,7 @@ constexpr int kSoftmaxRegs = 200;
 constexpr int kControlRegs = 96;
 static_assert(256 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * 168, "register re-balance exceeds the launch pool");
 constexpr int kKStages = 2;
-constexpr int kVStages = 3;
+constexpr int kVStages = 2;
 constexpr uint32_t kTileBytes = BM * D * 2;      // 32 KB
 constexpr uint32_t kBoxBytes = kTileBytes / 2;   // 16 KB: 128 rows x 64 halves
 constexpr uint32_t kPageBoxBytes = kPageSize * 64 * 2;  // 2 KB: 16 rows x 64 halves
