@@ -411,8 +411,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     mma_f16_ts(tmem + 256 + t * D, tmem + t * BN + kk * 8, bv + ((kk * 2048) >> 4),
                                idesc_o, (acc || kk > 0) ? 1u : 0u);
             };
-            auto wait = [&](uint64_t& bar, uint32_t parity) {
-                return __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar), parity, abort));
+            // The MMA warp sits in back-pressured MMA issue most of a step, so the
+            // barriers it checks next are usually complete by then; a complete one
+            // costs a non-blocking test here (a try_wait on it cost ~150-300 cycles,
+            // during which the tensor pipe's short queue ran dry).
+            auto wait = [&](uint64_t& bar, uint32_t parity) -> bool {
+                const uint32_t b = smem_u32(&bar);
+                if (__all_sync(0xffffffffu, mbar_test(b, parity)))
+                    return true;
+                return __all_sync(0xffffffffu, mbar_wait(b, parity, abort)) != 0;
             };
             bool ok = wait(ctl.q_full, 0) && wait(ctl.k_full[0], 0);
             if (ok) {
@@ -435,8 +442,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 // Operands first (usually long in place: the warp is idle until tile 0's
                 // P is ready anyway), so that nothing stands between PV0 and S0 below:
                 // each mbarrier wait costs the issuing warp of order a hundred cycles.
-                ok = wait(ctl.v_full[sv], phv) && (!more || wait(ctl.k_full[sk1], phk1)) &&
-                     wait(ctl.p_full[0], j & 1);
+                // usually all three are in place by now: one combined test first
+                ok = __all_sync(0xffffffffu, mbar_test(smem_u32(&ctl.v_full[sv]), phv) &&
+                                                 (!more || mbar_test(smem_u32(&ctl.k_full[sk1]), phk1)) &&
+                                                 mbar_test(smem_u32(&ctl.p_full[0]), j & 1)) ||
+                     (wait(ctl.v_full[sv], phv) && (!more || wait(ctl.k_full[sk1], phk1)) &&
+                      wait(ctl.p_full[0], j & 1));
                 if (!ok)
                     break;
                 if (PAGED && (j + 1) * BN > w.Lkv) {

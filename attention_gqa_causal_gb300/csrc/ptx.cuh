@@ -64,6 +64,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// Non-blocking test (never suspends): true once the phase with parity
+// `parity` of `bar` has completed.  A phase that is usually complete by the
+// time it is checked costs one test this way instead of a try_wait.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait until the phase with parity `parity` of `bar` has completed.
 // Gives up (returns false) after kWaitLimitNs / kWaitMaxIters, or as soon as
 // *abort is non-zero (another role of the CTA already gave up).
