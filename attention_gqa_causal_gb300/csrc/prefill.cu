@@ -21,7 +21,9 @@
 //   warps 4-7  softmax of Q tile 1
 //   warp  8    MMA warp (one lane issues) + TMEM allocation
 //   warp  9    TMA producer (one lane)
-//   warps 10-11 idle (they complete the third warpgroup)
+//   warp 10    relay (one lane): adds "V_j and K_{j+1} landed" to tile 0's P
+//              barrier, so the MMA warp checks one barrier per step
+//   warp 11    idle (it completes the third warpgroup)
 // After setup the warpgroups re-balance registers with setmaxnreg: the two
 // softmax warpgroups rise to 200 per thread, the MMA/TMA warpgroup drops to 96.
 // A CTA owns two 128-row Q tiles that read the same K/V: two query heads of
@@ -67,7 +69,8 @@ constexpr int D = kHeadDim;
 constexpr int kPagesPerTile = BN / kPageSize;
 constexpr int kMmaWarp = 8;
 constexpr int kTmaWarp = 9;
-constexpr int kThreads = 12 * 32;   // warps 10, 11 only complete the third warpgroup
+constexpr int kRelayWarp = 10;   // folds the step's operand waits into tile 0's P barrier
+constexpr int kThreads = 12 * 32;   // warp 11 only completes the third warpgroup
 // Registers per thread after the warpgroups re-balance (setmaxnreg): the MMA/TMA
 // warpgroup gives up what the softmax needs to keep a whole 128-key row of S
 // in flight (at 168 registers its exp loop serialises).  Launch pool: 384
@@ -282,7 +285,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(smem_u32(&ctl.s_full[t]), 1);
-            mbar_init(smem_u32(&ctl.p_full[t]), 128);
+            // tile 0's P barrier also takes the relay warp's arrival (operands in place)
+            mbar_init(smem_u32(&ctl.p_full[t]), t == 0 ? 129 : 128);
             mbar_init(smem_u32(&ctl.o_full[t]), 1);
             mbar_init(smem_u32(&ctl.epi_ready[t]), 128);
         }
@@ -382,6 +386,26 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                         mbar_wait(smem_u32(&ctl.v_full[s]), (c - 1) & 1, &no_abort);
                 }
             }
+        } else if (warp == kRelayWarp) {
+            // ------------------------------------------------------------ relay warp
+            // For each key tile j, once V_j and K_{j+1} have landed it adds the
+            // 129th arrival to p_full[0]'s phase j, so the MMA warp checks a single
+            // barrier before PV0(j) / S0(j+1).  It waits for phase j-1 to complete
+            // first, so that each phase gets exactly one of its arrivals.
+            if (lane == 0) {
+                bool ok = true;
+                for (int j = 0; j < w.n_kv && ok; ++j) {
+                    if (j > 0)
+                        ok = mbar_wait(smem_u32(&ctl.p_full[0]), (j - 1) & 1, abort);
+                    ok = ok && mbar_wait(smem_u32(&ctl.v_full[j % kVStages]), (j / kVStages) & 1, abort);
+                    if (ok && j + 1 < w.n_kv)
+                        ok = mbar_wait(smem_u32(&ctl.k_full[(j + 1) % kKStages]), ((j + 1) / kKStages) & 1, abort);
+                    if (ok)
+                        mbar_arrive(smem_u32(&ctl.p_full[0]));
+                }
+                if (!ok)
+                    flag_abort(&ctl, a.err);
+            }
         } else if (warp == kMmaWarp) {
             // ------------------------------------------------------------ MMA warp
             // The whole warp follows the schedule (so it can clear shared memory
@@ -435,19 +459,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             }
             for (int j = 0; j < w.n_kv && ok; ++j) {
                 const int sv = j % kVStages;
-                const uint32_t phv = (j / kVStages) & 1;
                 const int sk1 = (j + 1) % kKStages;
-                const uint32_t phk1 = ((j + 1) / kKStages) & 1;
                 const bool more = j + 1 < w.n_kv;
                 // Operands first (usually long in place: the warp is idle until tile 0's
                 // P is ready anyway), so that nothing stands between PV0 and S0 below:
                 // each mbarrier wait costs the issuing warp of order a hundred cycles.
-                // usually all three are in place by now: one combined test first
-                ok = __all_sync(0xffffffffu, mbar_test(smem_u32(&ctl.v_full[sv]), phv) &&
-                                                 (!more || mbar_test(smem_u32(&ctl.k_full[sk1]), phk1)) &&
-                                                 mbar_test(smem_u32(&ctl.p_full[0]), j & 1)) ||
-                     (wait(ctl.v_full[sv], phv) && (!more || wait(ctl.k_full[sk1], phk1)) &&
-                      wait(ctl.p_full[0], j & 1));
+                // p_full[0] completes once tile 0's P is written and the relay warp
+                // has seen V_j and K_{j+1} land (every barrier test here is a
+                // shared-memory access that queues behind the tensor core's operand
+                // reads; one test instead of three shortens the gap in which the
+                // tensor pipe's short queue runs dry)
+                ok = wait(ctl.p_full[0], j & 1);
                 if (!ok)
                     break;
                 if (PAGED && (j + 1) * BN > w.Lkv) {
