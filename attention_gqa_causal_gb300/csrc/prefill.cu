@@ -25,7 +25,8 @@
 //              barrier, so the MMA warp checks one barrier per step
 //   warp 11    idle (it completes the third warpgroup)
 // After setup the warpgroups re-balance registers with setmaxnreg: the two
-// softmax warpgroups rise to 200 per thread, the MMA/TMA warpgroup drops to 96.
+// softmax warpgroups rise to 200 per thread, the control warpgroup (MMA, TMA,
+// relay) drops to 96.
 // A CTA owns two 128-row Q tiles that read the same K/V: two query heads of
 // one GQA group over the same rows when the group size is even (identical
 // causal extents), else two consecutive row tiles of one head.  Per 128-key
@@ -46,8 +47,10 @@
 // TMEM: S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512) columns.
 // SMEM: Q0,Q1 (32 KB each), 2 K stages, 2 V stages (32 KB each), all
 // 128-byte swizzled as written by TMA boxes of 64 x 128 (contiguous K/V) or
-// 64 x 16 (one cache page).  Key tiles wholly above the diagonal are never
-// loaded or multiplied; only the diagonal tile is masked.
+// 64 x 16 (one cache page).  At the end O_t goes, normalised and swizzled,
+// into Q_t's buffer (free once the last S GEMM has completed) and out by TMA
+// store.  Key tiles wholly above the diagonal are never loaded or multiplied;
+// only the diagonal tile is masked.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -302,7 +305,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     tc_fence_after();
     const uint32_t tmem = ctl.tmem_base;
     // Whole warpgroups re-balance registers, each with one setmaxnreg and then only
-    // its own code: warps 8-11 (MMA, TMA, two idle) down, warps 0-7 (softmax) up.
+    // its own code: warps 8-11 (MMA, TMA, relay, idle) down, warps 0-7 (softmax) up.
     if (warp >= 8) {
         regs_decrease<kControlRegs>();
         if (warp == kTmaWarp) {
