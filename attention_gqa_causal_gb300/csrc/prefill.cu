@@ -129,9 +129,19 @@ template <bool PAGED>
 __device__ __forceinline__ Unit decode_unit(const PrefillArgs& a, int u)
 {
     Unit w;
-    // causal: longest row blocks first so short ones fill the tail of the grid
-    const int mb = a.causal ? a.n_mb - 1 - u / a.units_per_mb : u / a.units_per_mb;
-    int r = u % a.units_per_mb;
+    int mb, r;
+    if (!PAGED && !a.causal) {
+        // full attention, all units alike: (batch, kv head, pair) major, row
+        // blocks minor, so the CTAs that read the same K/V run together and
+        // fetch it from DRAM fewer times
+        r = u / a.n_mb;
+        mb = u % a.n_mb;
+    } else {
+        // causal (and paged): longest row blocks first so short ones fill the
+        // tail of the grid
+        mb = a.causal ? a.n_mb - 1 - u / a.units_per_mb : u / a.units_per_mb;
+        r = u % a.units_per_mb;
+    }
     const int per_g = a.units_per_mb / (a.B * a.H_kv);
     const int pr = r % per_g;
     r /= per_g;
