@@ -41,6 +41,5 @@ from ._binding import (  # noqa: F401
     attn_release_workspace,
     attn_version,
     load,
-    rope_table_entries,
     status_string,
 )

@@ -215,25 +215,13 @@ def attn_decode_paged_append(q, k_new, v_new, k_cache, v_cache, out, slot_mappin
 def attn_rope_cos_sin_table(cos_sin: torch.Tensor, base: float, stream=None) -> None:
     """Fill cos_sin [max_pos, 128] FP32 with the rotary table: the (cos, sin) of
     p * base^(-2j/128) for every position p and pair j, computed in FP64 on the
-    device and rounded once, in the entry order include/attn.h documents
-    (rope_table_entries() gives the plain [max_pos, 64] cos and sin)."""
+    device and rounded once, in the entry order include/attn.h documents."""
     if cos_sin.dim() != 2 or cos_sin.shape[1] != 128:
         raise ValueError("expected cos_sin [max_pos, 128] float32")
     ptr = _dev(cos_sin, "cos_sin", torch.float32)
     st = _stream(stream, cos_sin.device)
     _check(load().attn_rope_cos_sin_table(ptr, cos_sin.shape[0], 128, float(base), ctypes.c_void_p(st)),
            "attn_rope_cos_sin_table")
-
-
-def rope_table_entries(cos_sin):
-    """(cos, sin), each [max_pos, 64] in pair order, from a table filled by
-    attn_rope_cos_sin_table: entry (p, i, m) = p*32 + i*8 + m of its float4
-    view holds {cos j, cos j+1, sin j, sin j+1} for pair j = 8m + 2i."""
-    t = cos_sin.reshape(-1, 4, 8, 4)                 # [p, i, m, 4]
-    j_even = t[..., [0, 2]].permute(0, 2, 1, 3)      # [p, m, i, (cos, sin)] of pair 8m+2i
-    j_odd = t[..., [1, 3]].permute(0, 2, 1, 3)       # pair 8m+2i+1
-    pairs = torch.stack([j_even, j_odd], dim=3).reshape(t.shape[0], 64, 2)
-    return pairs[..., 0], pairs[..., 1]
 
 
 def _prologue_args(Q, K, q_weight, k_weight, cos_sin, positions):

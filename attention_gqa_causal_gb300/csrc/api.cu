@@ -7,6 +7,7 @@
 #include <mutex>
 #include <utility>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "attn.h"
@@ -15,6 +16,20 @@
 namespace {
 
 thread_local int t_last_cuda_error = 0;
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+template <typename Fn>
+Fn driver_fn(const char* name)
+{
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<Fn>(p);
+}
 
 int cuda_fail(cudaError_t e)
 {
@@ -37,10 +52,14 @@ int check_heads(int H_q, int H_kv)
     return ATTN_OK;
 }
 
-// Library-owned split-K scratch: one grow-only buffer per (device, stream).
+// Library-owned split-K scratch: one grow-only buffer per (device, stream),
+// tagged with the context it was allocated in.  A buffer from a context that
+// has since been replaced (cudaDeviceReset) went away with that context: it is
+// forgotten, never freed or used.
 struct Workspace {
     void* ptr = nullptr;
     size_t bytes = 0;
+    unsigned long long ctx = 0;
 };
 std::mutex g_ws_mutex;
 std::map<std::pair<int, uintptr_t>, Workspace> g_ws;
@@ -51,8 +70,14 @@ int get_workspace(size_t need, cudaStream_t stream, void** out)
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return cuda_fail(e);
+    unsigned long long ctx = 0;
+    e = attn::current_context_id(&ctx);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
     std::lock_guard<std::mutex> lock(g_ws_mutex);
     Workspace& w = g_ws[{dev, reinterpret_cast<uintptr_t>(stream)}];
+    if (w.ptr && w.ctx != ctx)
+        w = Workspace{};
     if (w.bytes < need) {
         if (w.ptr) {
             e = cudaFree(w.ptr);  // synchronous: earlier kernels using it have finished
@@ -68,6 +93,7 @@ int get_workspace(size_t need, cudaStream_t stream, void** out)
             return cuda_fail(e);
         }
         w.bytes = grow;
+        w.ctx = ctx;
     }
     *out = w.ptr;
     return ATTN_OK;
@@ -97,6 +123,32 @@ int validate_decode(const void* q, const void* k_cache, const void* v_cache, voi
 }  // namespace
 
 int attn::record_cuda_error(cudaError_t e) { return cuda_fail(e); }
+
+cudaError_t attn::current_context_id(unsigned long long* id)
+{
+    static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+    static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+    if (!get_current || !get_id)
+        return cudaErrorNotSupported;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS)
+        return cudaErrorDeviceUninitialized;
+    if (!ctx) {
+        // the runtime makes its primary context current on a thread lazily;
+        // selecting the current device again makes it current now
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess)
+            e = cudaSetDevice(dev);
+        if (e != cudaSuccess)
+            return e;
+        if (get_current(&ctx) != CUDA_SUCCESS || !ctx)
+            return cudaErrorDeviceUninitialized;
+    }
+    if (get_id(ctx, id) != CUDA_SUCCESS)
+        return cudaErrorDeviceUninitialized;
+    return cudaSuccess;
+}
 
 namespace {
 int prefill_checked(const void* Q, const void* K, const void* V, void* O, int B, int S, int H_q,
@@ -389,7 +441,11 @@ ATTN_API int attn_release_workspace(void)
     for (auto& kv : g_ws) {
         if (kv.second.ptr) {
             cudaError_t e = cudaSetDevice(kv.first.first);
+            unsigned long long ctx = 0;
             if (e == cudaSuccess)
+                e = attn::current_context_id(&ctx);
+            // a buffer of a context that no longer exists went away with it
+            if (e == cudaSuccess && ctx == kv.second.ctx)
                 e = cudaFree(kv.second.ptr);
             if (e != cudaSuccess && first == cudaSuccess)
                 first = e;

@@ -274,6 +274,15 @@ decode_splitk_kernel(const __half* __restrict__ q, const __half* __restrict__ k_
 #pragma unroll
         for (int w = 0; w < kDecodeWarps; ++w)
             M = fmaxf(M, sm_m[w][hh]);
+        const size_t row = (size_t)n * H_q + h0 + hh;
+        if (M == -CUDART_INF_F) {
+            // every page of this split had a negative block id (skipped and
+            // flagged above): an empty segment, which the combine step weighs 0
+            O_part[(row * n_split + split) * D + d] = 0.f;
+            if (d == 0)
+                lse_part[row * n_split + split] = -CUDART_INF_F;
+            continue;
+        }
         float Lsum = 0.f, acc = 0.f;
 #pragma unroll
         for (int w = 0; w < kDecodeWarps; ++w) {
@@ -281,7 +290,6 @@ decode_splitk_kernel(const __half* __restrict__ q, const __half* __restrict__ k_
             Lsum += c * sm_l[w][hh];
             acc += c * sm_o[w][hh][d];
         }
-        const size_t row = (size_t)n * H_q + h0 + hh;
         O_part[(row * n_split + split) * D + d] = acc / Lsum;
         if (d == 0)
             lse_part[row * n_split + split] = (M + __log2f(Lsum)) * kLn2;
@@ -392,6 +400,18 @@ int pick_heads_per_cta(int group)
     return 8;
 }
 
+// SMs of the current device; a GB300's 152 if it cannot be queried (the
+// workspace size may be asked for on a host without a GPU).
+int sm_count()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+        return n;
+    cudaGetLastError();   // leave no error of the failed query for a later launch check
+    return 152;
+}
+
 }  // namespace
 
 DecodePlan make_decode_plan(int num_seqs, int H_q, int H_kv, int max_blocks_per_seq,
@@ -408,8 +428,8 @@ DecodePlan make_decode_plan(int num_seqs, int H_q, int H_kv, int max_blocks_per_
     if (pages_per_split <= 0) {
         // 32 pages (512 tokens) per split measured best on both decode
         // workloads; smaller splits only when the grid would otherwise hold
-        // fewer than 16 CTAs per SM of a 152-SM GB300.
-        constexpr long long kTargetCtas = 16 * 152;
+        // fewer than 16 CTAs per SM of the current device.
+        const long long kTargetCtas = 16LL * sm_count();
         const long long units = (long long)num_seqs * H_kv * p.chunks;
         pages_per_split = 32;
         while (pages_per_split > 4 &&

@@ -59,6 +59,13 @@ cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* k_cache
 cudaError_t launch_lse_combine(const float* O_part, const float* lse_part, void* out, int R,
                                int n_split, cudaStream_t stream);
 
+// Process-unique id of the CUDA context current on this thread (the driver
+// never hands the same id to two contexts of one process, so a context that
+// replaced an earlier one, e.g. after cudaDeviceReset, is told apart from it).
+// If no context is current on the thread yet, the current device's primary
+// context is made current first.  Defined in api.cu.
+cudaError_t current_context_id(unsigned long long* id);
+
 // Store `e` as this thread's last CUDA error (attn_last_cuda_error) and
 // return ATTN_ERR_CUDA; defined in api.cu.
 int record_cuda_error(cudaError_t e);

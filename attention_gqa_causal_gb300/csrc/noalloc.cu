@@ -30,9 +30,18 @@ static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
-void* g_scratch_addr[kMaxDevices] = {};
+// Set-up per device: the device address of g_scratch, and the context it
+// belongs to.  A device whose context was replaced (cudaDeviceReset) has its
+// module loaded anew, possibly at another address, so the set-up runs again.
+struct ScratchSlot {
+    unsigned long long ctx = 0;
+    void* addr = nullptr;
+};
+ScratchSlot g_slot[kMaxDevices];
 
-// Device address of g_scratch on the current device, looked up once per device.
+// Device address of g_scratch on the current device.  cudaGetSymbolAddress
+// runs once per device and context (the first call on a device, and the
+// first after its context was replaced); later calls reuse the address.
 cudaError_t scratch_address(void** out)
 {
     int dev = 0;
@@ -41,15 +50,21 @@ cudaError_t scratch_address(void** out)
         return e;
     if (dev < 0 || dev >= kMaxDevices)
         return cudaErrorInvalidDevice;
+    unsigned long long ctx = 0;
+    e = attn::current_context_id(&ctx);
+    if (e != cudaSuccess)
+        return e;
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (!g_scratch_addr[dev]) {
+    ScratchSlot& s = g_slot[dev];
+    if (!s.addr || s.ctx != ctx) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_scratch);
         if (e != cudaSuccess)
             return e;
-        g_scratch_addr[dev] = p;
+        s.addr = p;
+        s.ctx = ctx;
     }
-    *out = g_scratch_addr[dev];
+    *out = s.addr;
     return cudaSuccess;
 }
 

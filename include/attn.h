@@ -122,7 +122,9 @@ ATTN_API int attn_debug_prefill_stall(const void* Q, const void* K, const void* 
  * flagged).
  * Scratch for the split-K partials comes from a library-owned grow-only
  * buffer per (device, stream); growing it calls cudaMalloc/cudaFree (which
- * synchronise the device).  Use attn_decode_paged_ws to pass your own.
+ * synchronise the device).  A buffer of a context that has been replaced
+ * since (cudaDeviceReset) is forgotten and a new one allocated.  Use
+ * attn_decode_paged_ws to pass your own.
  */
 ATTN_API int attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
                                void* out, const int* block_tables, const int* seq_lens,
@@ -132,8 +134,9 @@ ATTN_API int attn_decode_paged(const void* q, const void* k_cache, const void* v
 /*
  * Bytes of scratch attn_decode_paged_ws needs for these sizes.
  * pages_per_split: KV pages per split-K work unit.  <= 0 picks the default: 32,
- * halved (down to 4) while the grid would hold fewer than 2432 CTAs.
- * Returns 0 for invalid sizes.
+ * halved (down to 4) while the grid would hold fewer than 16 CTAs per SM of
+ * the current device (2432 on a 152-SM GB300; 152 SMs are assumed when the
+ * device cannot be queried).  Returns 0 for invalid sizes.
  */
 ATTN_API size_t attn_decode_paged_workspace_bytes(int num_seqs, int H_q, int H_kv, int D,
                                                   int max_blocks_per_seq, int block_size,
@@ -167,7 +170,9 @@ ATTN_API int attn_decode_paged_ws(const void* q, const void* k_cache, const void
  *    pages_per_split = 0) exceeds ATTN_NOALLOC_SCRATCH_BYTES is refused with
  *    ATTN_ERR_WORKSPACE before anything is launched.
  *  - The first call on a device looks up the buffer's device address with
- *    cudaGetSymbolAddress; make that first call before any stream capture.
+ *    cudaGetSymbolAddress (so does the first call after the device's context
+ *    was replaced, e.g. by cudaDeviceReset); make that first call before any
+ *    stream capture.
  *  - Every call on a device shares the one buffer, which keeps the last
  *    call's contents.  Nothing needs clearing (each partial that is read is
  *    written earlier in the same call), but calls that overlap on the GPU

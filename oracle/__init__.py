@@ -244,6 +244,33 @@ def prefill_paged(Q, k_cache, v_cache, cu_seqlens_q, seq_lens_kv, block_tables, 
     return (O, lse) if with_lse else O
 
 
+def prefill_paged_rows(Q, k_cache, v_cache, cu_seqlens_q, seq_lens_kv, block_tables, rows,
+                       causal=True, with_lse=False):
+    """Oracle rows (b, i, h) of prefill_paged only (query i of sequence b's
+    chunk, head h): returns [n_rows, D] float64."""
+    Q, kc, vc = _half(Q), _half(k_cache), _half(v_cache)
+    cu, sl, bt = _i32(cu_seqlens_q), _i32(seq_lens_kv), _i32(block_tables)
+    total_q, H_q, D = Q.shape
+    B = sl.shape[0]
+    assert cu.shape == (B + 1,) and cu[-1] == total_q
+    rows = _i32(np.asarray(rows, np.int32).reshape(-1, 3))
+    lq = np.diff(cu)
+    assert np.all((rows[:, 0] >= 0) & (rows[:, 0] < B)), "sequence index out of range"
+    assert np.all((rows[:, 1] >= 0) & (rows[:, 1] < lq[rows[:, 0]])), "query index out of range"
+    assert np.all((rows[:, 2] >= 0) & (rows[:, 2] < H_q)), "head index out of range"
+    H_kv, bs = kc.shape[1], kc.shape[2]
+    out = np.empty((rows.shape[0], D), np.float64)
+    lse = np.empty((rows.shape[0],), np.float64)
+    lib = _load()
+    p, i = ctypes.c_void_p, ctypes.c_int
+    lib.oracle_prefill_paged_rows.argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, i, p, i, p, p]
+    lib.oracle_prefill_paged_rows.restype = None
+    lib.oracle_prefill_paged_rows(_ptr(Q), _ptr(kc), _ptr(vc), _ptr(cu), _ptr(sl), _ptr(bt), B,
+                                  H_q, H_kv, D, bt.shape[1], bs, int(bool(causal)), _ptr(rows),
+                                  rows.shape[0], _ptr(out), _ptr(lse))
+    return (out, lse) if with_lse else out
+
+
 def qk_norm_rope(x, weight, positions, base, eps=1e-6):
     """Per-head RMSNorm (skipped when ``weight`` is None) then NeoX rotary
     embedding of x [T, H, D] at ``positions`` [T]; float64 result."""

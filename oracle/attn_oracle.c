@@ -399,6 +399,29 @@ int oracle_kv_append(const uint16_t *k_new, const uint16_t *v_new, uint16_t *k_c
  * the paged layout of the "Paged Attention -- Decode" header; the causal rule
  * is the prefill one, shifted by the cached prefix.
  */
+/* One output row (query i of sequence b, head h) of the paged prefill. */
+static void prefill_paged_row(const uint16_t *Q, const uint16_t *k_cache,
+                              const uint16_t *v_cache, const int32_t *cu_seqlens_q,
+                              const int32_t *seq_lens_kv, const int32_t *block_tables, int H_q,
+                              int H_kv, int D, int max_blocks_per_seq, int block_size,
+                              int causal, int b, int i, int h, double *scores, double *o,
+                              double *lse)
+{
+    const int Lq = cu_seqlens_q[b + 1] - cu_seqlens_q[b];
+    const int Lkv = seq_lens_kv[b];
+    paged_ctx c;
+    c.kc = k_cache;
+    c.vc = v_cache;
+    c.table = block_tables + (long)b * max_blocks_per_seq;
+    c.H_kv = H_kv;
+    c.bs = block_size;
+    c.D = D;
+    c.g = (int)(((long)h * H_kv) / H_q);
+    const int n = causal ? Lkv - Lq + i + 1 : Lkv;
+    const long row = (long)cu_seqlens_q[b] + i;
+    attend_one(Q + (row * H_q + h) * D, D, n, paged_key, paged_val, &c, scores, o, lse);
+}
+
 void oracle_prefill_paged(const uint16_t *Q, const uint16_t *k_cache, const uint16_t *v_cache,
                           const int32_t *cu_seqlens_q, const int32_t *seq_lens_kv,
                           const int32_t *block_tables, int B, int H_q, int H_kv, int D,
@@ -418,23 +441,40 @@ void oracle_prefill_paged(const uint16_t *Q, const uint16_t *k_cache, const uint
             int b = 0;
             while (cu_seqlens_q[b + 1] <= row)
                 b++;
-            const int i = row - cu_seqlens_q[b];
-            const int Lq = cu_seqlens_q[b + 1] - cu_seqlens_q[b];
-            const int Lkv = seq_lens_kv[b];
-            paged_ctx c;
-            c.kc = k_cache;
-            c.vc = v_cache;
-            c.table = block_tables + (long)b * max_blocks_per_seq;
-            c.H_kv = H_kv;
-            c.bs = block_size;
-            c.D = D;
-            c.g = (int)(((long)h * H_kv) / H_q);
-            const int n = causal ? Lkv - Lq + i + 1 : Lkv;
             double l;
-            attend_one(Q + ((long)row * H_q + h) * D, D, n, paged_key, paged_val, &c, scores,
-                       O + r * D, &l);
+            prefill_paged_row(Q, k_cache, v_cache, cu_seqlens_q, seq_lens_kv, block_tables, H_q,
+                              H_kv, D, max_blocks_per_seq, block_size, causal, b,
+                              row - cu_seqlens_q[b], h, scores, O + r * D, &l);
             if (lse)
                 lse[r] = l;
+        }
+        free(scores);
+    }
+}
+
+/*
+ * Selected rows of the paged prefill.  rows: n_rows triples (b, i, h), query i
+ * of sequence b's chunk; O_rows: [n_rows, D]; lse_rows: [n_rows] or NULL.
+ */
+void oracle_prefill_paged_rows(const uint16_t *Q, const uint16_t *k_cache,
+                               const uint16_t *v_cache, const int32_t *cu_seqlens_q,
+                               const int32_t *seq_lens_kv, const int32_t *block_tables, int B,
+                               int H_q, int H_kv, int D, int max_blocks_per_seq, int block_size,
+                               int causal, const int32_t *rows, int n_rows, double *O_rows,
+                               double *lse_rows)
+{
+    const int L = max_len(seq_lens_kv, B);
+#pragma omp parallel
+    {
+        double *scores = (double *)malloc(sizeof(double) * L);
+#pragma omp for schedule(dynamic, 1)
+        for (int r = 0; r < n_rows; r++) {
+            double l;
+            prefill_paged_row(Q, k_cache, v_cache, cu_seqlens_q, seq_lens_kv, block_tables, H_q,
+                              H_kv, D, max_blocks_per_seq, block_size, causal, rows[3 * r],
+                              rows[3 * r + 1], rows[3 * r + 2], scores, O_rows + (long)r * D, &l);
+            if (lse_rows)
+                lse_rows[r] = l;
         }
         free(scores);
     }

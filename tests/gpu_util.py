@@ -37,3 +37,15 @@ def assert_close(gpu, ref, what="", max_abs=MAX_ABS, mean_abs=MEAN_ABS):
 def device_error_clean():
     import attention_gqa_causal_gb300 as ag
     return ag.attn_get_device_error(reset=True) == 0
+
+
+def rope_table_entries(cos_sin):
+    """(cos, sin), each [max_pos, 64] in pair order, from a table filled by
+    attn_rope_cos_sin_table: entry (p, i, m) = p*32 + i*8 + m of its float4
+    view holds {cos j, cos j+1, sin j, sin j+1} for pair j = 8m + 2i (the
+    entry order include/attn.h documents)."""
+    t = cos_sin.reshape(-1, 4, 8, 4)                 # [p, i, m, 4]
+    j_even = t[..., [0, 2]].permute(0, 2, 1, 3)      # [p, m, i, (cos, sin)] of pair 8m+2i
+    j_odd = t[..., [1, 3]].permute(0, 2, 1, 3)       # pair 8m+2i+1
+    pairs = torch.stack([j_even, j_odd], dim=3).reshape(t.shape[0], 64, 2)
+    return pairs[..., 0], pairs[..., 1]

@@ -392,6 +392,26 @@ def test_prefill_paged_noncausal_and_decode_special_case():
         np.testing.assert_allclose(out[cu[b]:cu[b + 1]], ref, atol=1e-12)
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_prefill_paged_rows_match_sdpa(causal):
+    # selected rows (b, i, h) against torch float64 SDPA over each sequence's own keys
+    rng = np.random.default_rng(52)
+    lens_kv, lens_q, H_q, H_kv, D = [40, 23, 70], [9, 23, 5], 6, 2, 16
+    K, V, kc, vc, table, Q, cu, skv = _paged_problem(rng, lens_kv, lens_q, H_q, H_kv, D)
+    rows = np.array([(b, i, h) for b in range(3) for i in range(lens_q[b]) for h in range(H_q)
+                     if (b * 7 + i * 3 + h) % 4 == 0], np.int32)
+    got = oracle.prefill_paged_rows(Q, kc, vc, cu, skv, table, rows, causal=causal)
+    for r, (b, i, h) in enumerate(rows):
+        Lkv, Lq = lens_kv[b], lens_q[b]
+        if causal:
+            Qfull = np.zeros((1, Lkv, H_q, D), np.float16)
+            Qfull[0, Lkv - Lq:] = Q[cu[b]:cu[b + 1]]
+            ref = _sdpa(Qfull, K[b][None], V[b][None], causal=True)[0, Lkv - Lq + i, h]
+        else:
+            ref = _sdpa(Q[cu[b] + i][None, None], K[b][None], V[b][None], causal=False)[0, 0, h]
+        np.testing.assert_allclose(got[r], ref, atol=1e-12)
+
+
 # ------------------------------------------------ QK-norm + RoPE prologue
 
 ROPE_BASE = 1.0e6

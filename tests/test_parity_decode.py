@@ -204,3 +204,27 @@ def test_empty_batch_noop_and_library_workspace_release():
     sl = torch.zeros(0, dtype=torch.int32, device="cuda")
     ag.attn_decode_paged(q, kc, kc, q.clone(), bt, sl)
     ag.attn_release_workspace()
+
+
+@pytest.mark.parametrize("pps", [None, 4])
+def test_split_of_negative_block_ids_contributes_nothing(pps):
+    # sequence 0: pages 4..7 (one whole split at 4 pages per split) hold -1;
+    # sequence 1: every page holds -1; sequence 2 is clean.  The skipped pages
+    # drop out of the softmax, so the result is the oracle's over the pages
+    # that remain (listed contiguously in a compacted table).
+    lens = [315, 100, 500]
+    inp = make(len(lens), 16, 8, lens, max_blocks=32, seed=13)
+    bt = inp.block_tables.copy()
+    bt[0, 4:8] = -1
+    bt[1, :7] = -1
+    out = run_decode(W.DecodeInputs(inp.q, inp.k_cache, inp.v_cache, bt, inp.seq_lens),
+                     pages_per_split=pps)
+    assert ag.attn_get_device_error(reset=True) == 2
+    keep0 = [p for p in range(20) if not 4 <= p < 8]
+    ct = np.full_like(bt, -1)
+    ct[0, :len(keep0)] = inp.block_tables[0, keep0]
+    ct[2] = inp.block_tables[2]
+    cl = np.array([315 - 64, 0, 500], np.int32)
+    ref = oracle.decode_paged(inp.q, inp.k_cache, inp.v_cache, ct, cl)
+    assert np.all(out[1] == 0)
+    assert_close(out, ref, f"negative-id split, pages_per_split={pps}")

@@ -61,24 +61,42 @@ def test_qwen_shape_full_compare():
     assert device_error_clean()
 
 
-def _sample_rows(cfg, n, seed):
+def stratified_rows(B, S, H_q, seed, diag_blocks, diag_heads):
+    """Rows (b, i, h) that reach every CTA of a full-size launch on both of its
+    Q tiles: one random row in every (b, 128-row block, q head), plus every
+    row of the listed 128-row blocks (diagonal tiles under the causal mask)
+    for the listed heads of each batch entry."""
     rng = np.random.default_rng(seed)
-    rows = [(b, i, h) for b in range(cfg.B) for i in (0, 1, 127, 128, cfg.S - 129, cfg.S - 1)
-            for h in (0, cfg.H_q - 1)]
-    rows += [(int(rng.integers(cfg.B)), int(rng.integers(cfg.S)), int(rng.integers(cfg.H_q)))
-             for _ in range(n)]
-    return np.array(rows, np.int32)
+    n_mb = (S + 127) // 128
+    b, mb, h = np.meshgrid(np.arange(B), np.arange(n_mb), np.arange(H_q), indexing="ij")
+    b, mb, h = b.ravel(), mb.ravel(), h.ravel()
+    width = np.minimum(128, S - mb * 128)
+    i = mb * 128 + (rng.random(b.size) * width).astype(np.int64)
+    rows = [np.stack([b, i, h], 1)]
+    for bb in range(B):
+        for blk in diag_blocks:
+            r = np.arange(blk * 128, min(S, blk * 128 + 128))
+            for hh in diag_heads:
+                rows.append(np.stack([np.full_like(r, bb), r, np.full_like(r, hh)], 1))
+    return np.unique(np.concatenate(rows).astype(np.int32), axis=0)
 
 
 @pytest.mark.parametrize("cfg", [W.PREFILL_LONG, W.PREFILL_LONG_FULL], ids=lambda c: c.name)
-def test_long_workload_sampled_rows(cfg):
+def test_long_workload_stratified_rows(cfg):
+    # the launch the benchmark times (B 2, S 8192, H 32/8), every CTA checked
     Q, K, V = W.prefill_inputs(cfg, seed=0)
-    O = run_prefill(Q, K, V, cfg.causal)
-    rows = _sample_rows(cfg, 160, seed=1)
+    O = torch.full(Q.shape, float("nan"), dtype=torch.float16, device="cuda")
+    ag.attn_prefill(dev(Q), dev(K), dev(V), O, causal=cfg.causal)
+    torch.cuda.synchronize()
+    O = host(O)
+    n_mb = cfg.S // 128
+    rows = stratified_rows(cfg.B, cfg.S, cfg.H_q, seed=1, diag_blocks=(0, n_mb // 2, n_mb - 1),
+                           diag_heads=(0, 13, cfg.H_q - 1))
+    assert len(rows) >= cfg.B * n_mb * cfg.H_q
     ref = oracle.prefill_rows(Q, K, V, rows, causal=cfg.causal)
     got = O[rows[:, 0], rows[:, 1], rows[:, 2]]
-    assert_close(got, ref, cfg.name)
-    assert np.isfinite(O.astype(np.float32)).all()
+    assert_close(got, ref, f"{cfg.name}: {len(rows)} stratified rows")
+    assert np.isfinite(O.astype(np.float32)).all(), "rows left unwritten"
     assert device_error_clean()
 
 

@@ -15,6 +15,7 @@ import oracle
 import workloads as W
 from gpu_util import assert_close, dev, device_error_clean, host
 from test_oracle_pins import _paged_problem
+from test_parity_prefill import stratified_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -83,6 +84,24 @@ def test_chunked_prefill_workload_sampled():
     out = run(Q, kc, vc, cu, skv, table)
     ref = oracle.prefill_paged(Q, kc, vc, cu, skv, table)
     assert_close(out, ref, "chunked prefill")
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_chunked_prefill_bench_workload_stratified(causal):
+    # the benchmark's launch: 4 x (6144 cached + 2048 new), H 32/8, one random row
+    # per (sequence, 128-row block, head) plus all rows of the first and last
+    # chunk blocks for three heads: every CTA of the launch is checked
+    cfg = W.CHUNKED_PREFILL
+    Q, kc, vc, cu, skv, table = W.chunked_prefill_inputs(cfg, seed=0)
+    out = run(Q, kc, vc, cu, skv, table, causal=causal, max_q=cfg.chunk)
+    assert np.isfinite(out.astype(np.float32)).all(), "rows left unwritten"
+    n_mb = cfg.chunk // 128
+    rows = stratified_rows(cfg.num_seqs, cfg.chunk, cfg.H_q, seed=2, diag_blocks=(0, n_mb - 1),
+                           diag_heads=(0, 17, cfg.H_q - 1))
+    ref = oracle.prefill_paged_rows(Q, kc, vc, cu, skv, table, rows, causal=causal)
+    got = out[cu[rows[:, 0]] + rows[:, 1], rows[:, 2]]
+    assert_close(got, ref, f"{cfg.name} causal={causal}: {len(rows)} stratified rows")
+    assert device_error_clean()
 
 
 def test_device_length_checks():

@@ -13,7 +13,7 @@ import torch
 import attention_gqa_causal_gb300 as ag
 import oracle
 import workloads as W
-from gpu_util import assert_close, dev, device_error_clean, host
+from gpu_util import assert_close, dev, device_error_clean, host, rope_table_entries
 from test_oracle_pins import _paged_problem
 
 pytestmark = pytest.mark.gpu
@@ -46,7 +46,7 @@ def rand_weights(rng, D=128):
 
 def test_table_matches_fp64_cos_sin():
     max_pos = 70000
-    c, s = (host(x).astype(np.float64) for x in ag.rope_table_entries(table(max_pos)))
+    c, s = (host(x).astype(np.float64) for x in rope_table_entries(table(max_pos)))
     p = np.arange(max_pos, dtype=np.float64)[:, None]
     a = p * BASE ** (-2.0 * np.arange(64) / 128)
     # one rounding of the exact value to FP32 (relative 2^-24, |cos|,|sin| <= 1)
