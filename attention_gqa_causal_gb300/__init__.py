@@ -35,6 +35,7 @@ from ._binding import (  # noqa: F401
     attn_lse_combine,
     attn_prefill,
     attn_prefill_paged,
+    attn_prefill_paged_qk_norm_rope,
     attn_qk_norm_rope,
     attn_qk_norm_rope_append,
     attn_rope_cos_sin_table,

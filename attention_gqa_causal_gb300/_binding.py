@@ -28,7 +28,7 @@ EXPORTED = [
     "attn_get_device_error", "attn_last_cuda_error", "attn_status_string", "attn_version",
     "attn_decode_paged_noalloc", "attn_debug_prefill_stall", "attn_kv_append",
     "attn_decode_paged_append", "attn_prefill_paged", "attn_rope_cos_sin_table",
-    "attn_qk_norm_rope", "attn_qk_norm_rope_append",
+    "attn_qk_norm_rope", "attn_qk_norm_rope_append", "attn_prefill_paged_qk_norm_rope",
 ]
 
 # Size of the scratch buffer compiled into the library for attn_decode_paged_noalloc.
@@ -79,6 +79,8 @@ def load():
             lib.attn_qk_norm_rope.argtypes = [p, p, p, p, p, i, p, i, i, i, i, f, p]
             lib.attn_qk_norm_rope_append.argtypes = [p, p, p, p, p, p, i, p, p, p, p, i, i, i, i, i,
                                                      ll, f, p]
+            lib.attn_prefill_paged_qk_norm_rope.argtypes = [p, p, p, p, p, p, p, p, p, i, f, i, i, i,
+                                                            i, i, i, i, i, ll, i, p]
             _lib = lib
     return _lib
 
@@ -127,25 +129,51 @@ def attn_prefill(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.Ten
                                ctypes.c_void_p(st)), "attn_prefill")
 
 
+def _paged_prefill_args(Q, k_cache, v_cache, O, cu_seqlens_q, seq_lens_kv, block_tables):
+    if Q.dim() != 3 or O.shape != Q.shape or k_cache.dim() != 4 or v_cache.shape != k_cache.shape:
+        raise ValueError("expected Q,O [total_q,H_q,D] and caches [num_blocks,H_kv,block_size,D]")
+    B = seq_lens_kv.shape[0]
+    if cu_seqlens_q.shape != (B + 1,) or block_tables.dim() != 2 or block_tables.shape[0] != B:
+        raise ValueError("expected cu_seqlens_q [B+1], seq_lens_kv [B], block_tables [B, max_blocks]")
+    return [_dev(Q, "Q", torch.float16), _dev(k_cache, "k_cache", torch.float16),
+            _dev(v_cache, "v_cache", torch.float16), _dev(O, "O", torch.float16),
+            _dev(cu_seqlens_q, "cu_seqlens_q", torch.int32), _dev(seq_lens_kv, "seq_lens_kv", torch.int32),
+            _dev(block_tables, "block_tables", torch.int32)]
+
+
 def attn_prefill_paged(Q, k_cache, v_cache, O, cu_seqlens_q, seq_lens_kv, block_tables,
                        max_seqlen_q: int, causal: bool = True, stream=None) -> None:
     """Prefill of packed query chunks (Q, O [total_q, H_q, D]; cu_seqlens_q [B+1])
     against a paged cache holding seq_lens_kv[b] keys per sequence (its last
     L_q keys are the chunk's own): query i sits at position L_kv - L_q + i."""
-    if Q.dim() != 3 or O.shape != Q.shape or k_cache.dim() != 4 or v_cache.shape != k_cache.shape:
-        raise ValueError("expected Q,O [total_q,H_q,D] and caches [num_blocks,H_kv,block_size,D]")
+    ptrs = _paged_prefill_args(Q, k_cache, v_cache, O, cu_seqlens_q, seq_lens_kv, block_tables)
     total_q, H_q, D = Q.shape
-    B = seq_lens_kv.shape[0]
-    if cu_seqlens_q.shape != (B + 1,) or block_tables.dim() != 2 or block_tables.shape[0] != B:
-        raise ValueError("expected cu_seqlens_q [B+1], seq_lens_kv [B], block_tables [B, max_blocks]")
-    ptrs = [_dev(Q, "Q", torch.float16), _dev(k_cache, "k_cache", torch.float16),
-            _dev(v_cache, "v_cache", torch.float16), _dev(O, "O", torch.float16),
-            _dev(cu_seqlens_q, "cu_seqlens_q", torch.int32), _dev(seq_lens_kv, "seq_lens_kv", torch.int32),
-            _dev(block_tables, "block_tables", torch.int32)]
     st = _stream(stream, Q.device)
-    _check(load().attn_prefill_paged(*ptrs, B, int(max_seqlen_q), total_q, H_q, k_cache.shape[1], D,
-                                     block_tables.shape[1], k_cache.shape[2], k_cache.shape[0],
-                                     int(bool(causal)), ctypes.c_void_p(st)), "attn_prefill_paged")
+    _check(load().attn_prefill_paged(*ptrs, seq_lens_kv.shape[0], int(max_seqlen_q), total_q, H_q,
+                                     k_cache.shape[1], D, block_tables.shape[1], k_cache.shape[2],
+                                     k_cache.shape[0], int(bool(causal)), ctypes.c_void_p(st)),
+           "attn_prefill_paged")
+
+
+def attn_prefill_paged_qk_norm_rope(Q, k_cache, v_cache, O, cu_seqlens_q, seq_lens_kv,
+                                    block_tables, q_weight, cos_sin, max_seqlen_q: int,
+                                    eps: float = 1e-6, causal: bool = True, stream=None) -> None:
+    """attn_prefill_paged on raw query projections: each query row is first
+    normalised (q_weight [D], None = no norm) and rotated at its position with
+    the cos/sin table [max_pos, D] inside the kernel; Q is only read."""
+    ptrs = _paged_prefill_args(Q, k_cache, v_cache, O, cu_seqlens_q, seq_lens_kv, block_tables)
+    total_q, H_q, D = Q.shape
+    if cos_sin.dim() != 2 or cos_sin.shape[1] != D:
+        raise ValueError("expected cos_sin [max_pos, D] float32")
+    if q_weight is not None and q_weight.shape != (D,):
+        raise ValueError("expected q_weight [D]")
+    w = None if q_weight is None else _dev(q_weight, "q_weight", torch.float16)
+    cs = _dev(cos_sin, "cos_sin", torch.float32)
+    st = _stream(stream, Q.device)
+    _check(load().attn_prefill_paged_qk_norm_rope(
+        *ptrs, w, cs, cos_sin.shape[0], float(eps), seq_lens_kv.shape[0], int(max_seqlen_q), total_q,
+        H_q, k_cache.shape[1], D, block_tables.shape[1], k_cache.shape[2], k_cache.shape[0],
+        int(bool(causal)), ctypes.c_void_p(st)), "attn_prefill_paged_qk_norm_rope")
 
 
 def attn_debug_prefill_stall(Q, K, V, O, stall_tile: int, causal: bool = True, stream=None) -> None:
@@ -225,18 +253,20 @@ def attn_rope_cos_sin_table(cos_sin: torch.Tensor, base: float, stream=None) -> 
 
 
 def _prologue_args(Q, K, q_weight, k_weight, cos_sin, positions):
-    if Q.dim() != 3 or K.dim() != 3 or K.shape[0] != Q.shape[0] or K.shape[2] != Q.shape[2]:
+    """Q may be None (keys-only form of the append)."""
+    if K.dim() != 3 or (Q is not None and (Q.dim() != 3 or K.shape[0] != Q.shape[0] or K.shape[2] != Q.shape[2])):
         raise ValueError("expected Q [T,H_q,D] and K [T,H_kv,D]")
-    if cos_sin.dim() != 2 or cos_sin.shape[1] != Q.shape[2]:
+    D = K.shape[2]
+    if cos_sin.dim() != 2 or cos_sin.shape[1] != D:
         raise ValueError("expected cos_sin [max_pos, D] float32")
-    if positions.shape != (Q.shape[0],):
+    if positions.shape != (K.shape[0],):
         raise ValueError("expected positions [T] int32")
     w = []
     for name, t in (("q_weight", q_weight), ("k_weight", k_weight)):
         if t is None:
             w.append(None)
         else:
-            if t.shape != (Q.shape[2],):
+            if t.shape != (D,):
                 raise ValueError(f"expected {name} [D]")
             w.append(_dev(t, name, torch.float16))
     return w, _dev(cos_sin, "cos_sin", torch.float32), _dev(positions, "positions", torch.int32)
@@ -246,6 +276,8 @@ def attn_qk_norm_rope(Q, K, q_weight, k_weight, cos_sin, positions, eps: float =
                       stream=None) -> None:
     """In place: per-head RMSNorm (weight None = none) then NeoX RoPE of
     Q [T,H_q,128] and K [T,H_kv,128] at positions [T]."""
+    if Q is None:
+        raise ValueError("attn_qk_norm_rope rewrites Q in place: Q is required")
     w, cs, pos = _prologue_args(Q, K, q_weight, k_weight, cos_sin, positions)
     T, H_q, D = Q.shape
     st = _stream(stream, Q.device)
@@ -255,21 +287,26 @@ def attn_qk_norm_rope(Q, K, q_weight, k_weight, cos_sin, positions, eps: float =
 
 
 def attn_qk_norm_rope_append(Q, K, V, q_weight, k_weight, cos_sin, positions, slot_mapping,
-                             k_cache, v_cache, eps: float = 1e-6, stream=None) -> None:
+                             k_cache, v_cache, eps: float = 1e-6, stream=None, H_q: int = 0) -> None:
     """Q normalised and rotated in place; K normalised and rotated, and V as is,
-    written to their paged slots (int64 slot_mapping, -1 skipped)."""
+    written to their paged slots (int64 slot_mapping, -1 skipped).  Q=None
+    processes keys and values only (the queries' part then runs inside
+    attn_prefill_paged_qk_norm_rope); H_q is the query head count for the
+    checks in that case (it defaults to the KV head count)."""
     w, cs, pos = _prologue_args(Q, K, q_weight, k_weight, cos_sin, positions)
-    T, H_q, D = Q.shape
+    T, H_kv, D = K.shape
+    hq = Q.shape[1] if Q is not None else (H_q or H_kv)
     if V.shape != K.shape or k_cache.dim() != 4 or v_cache.shape != k_cache.shape:
         raise ValueError("expected V like K and caches [num_blocks,H_kv,block_size,D]")
     if slot_mapping.shape != (T,):
         raise ValueError("expected slot_mapping [T]")
-    st = _stream(stream, Q.device)
+    st = _stream(stream, K.device)
+    q = None if Q is None else _dev(Q, "Q", torch.float16)
     _check(load().attn_qk_norm_rope_append(
-        _dev(Q, "Q", torch.float16), _dev(K, "K", torch.float16), _dev(V, "V", torch.float16),
+        q, _dev(K, "K", torch.float16), _dev(V, "V", torch.float16),
         w[0], w[1], cs, cos_sin.shape[0], pos, _dev(slot_mapping, "slot_mapping", torch.int64),
-        _dev(k_cache, "k_cache", torch.float16), _dev(v_cache, "v_cache", torch.float16), T, H_q,
-        K.shape[1], D, k_cache.shape[2], k_cache.shape[0], float(eps), ctypes.c_void_p(st)),
+        _dev(k_cache, "k_cache", torch.float16), _dev(v_cache, "v_cache", torch.float16), T, hq,
+        H_kv, D, k_cache.shape[2], k_cache.shape[0], float(eps), ctypes.c_void_p(st)),
         "attn_qk_norm_rope_append")
 
 

@@ -172,21 +172,11 @@ int prefill_checked(const void* Q, const void* K, const void* V, void* O, int B,
     const cudaError_t e = attn::launch_prefill(Q, K, V, O, B, S, H_q, H_kv, causal, stall_tile, stream);
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
-}  // namespace
-
-extern "C" {
-
-ATTN_API int attn_prefill(const void* Q, const void* K, const void* V, void* O, int B, int S,
-                          int H_q, int H_kv, int D, int causal, cudaStream_t stream)
-{
-    return prefill_checked(Q, K, V, O, B, S, H_q, H_kv, D, causal, -1, stream);
-}
-
-ATTN_API int attn_prefill_paged(const void* Q, const void* k_cache, const void* v_cache, void* O,
-                                const int* cu_seqlens_q, const int* seq_lens_kv,
-                                const int* block_tables, int B, int max_seqlen_q, int total_q,
-                                int H_q, int H_kv, int D, int max_blocks_per_seq, int block_size,
-                                long long num_blocks, int causal, cudaStream_t stream)
+int prefill_paged_checked(const void* Q, const void* k_cache, const void* v_cache, void* O,
+                          const int* cu_seqlens_q, const int* seq_lens_kv, const int* block_tables,
+                          int B, int max_seqlen_q, int total_q, int H_q, int H_kv, int D,
+                          int max_blocks_per_seq, int block_size, long long num_blocks, int causal,
+                          const attn::QueryPrologue* qp, cudaStream_t stream)
 {
     if (B < 0 || max_seqlen_q < 0 || total_q < 0 || max_blocks_per_seq < 1 || num_blocks < 0 ||
         check_heads(H_q, H_kv) != ATTN_OK)
@@ -208,8 +198,53 @@ ATTN_API int attn_prefill_paged(const void* Q, const void* k_cache, const void* 
         return ATTN_ERR_INVALID_ARG;
     const cudaError_t e = attn::launch_prefill_paged(
         Q, k_cache, v_cache, O, cu_seqlens_q, seq_lens_kv, block_tables, B, max_seqlen_q, total_q,
-        H_q, H_kv, max_blocks_per_seq, num_blocks, causal, stream);
+        H_q, H_kv, max_blocks_per_seq, num_blocks, causal, qp, stream);
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+}  // namespace
+
+extern "C" {
+
+ATTN_API int attn_prefill(const void* Q, const void* K, const void* V, void* O, int B, int S,
+                          int H_q, int H_kv, int D, int causal, cudaStream_t stream)
+{
+    return prefill_checked(Q, K, V, O, B, S, H_q, H_kv, D, causal, -1, stream);
+}
+
+ATTN_API int attn_prefill_paged(const void* Q, const void* k_cache, const void* v_cache, void* O,
+                                const int* cu_seqlens_q, const int* seq_lens_kv,
+                                const int* block_tables, int B, int max_seqlen_q, int total_q,
+                                int H_q, int H_kv, int D, int max_blocks_per_seq, int block_size,
+                                long long num_blocks, int causal, cudaStream_t stream)
+{
+    return prefill_paged_checked(Q, k_cache, v_cache, O, cu_seqlens_q, seq_lens_kv, block_tables, B,
+                                 max_seqlen_q, total_q, H_q, H_kv, D, max_blocks_per_seq,
+                                 block_size, num_blocks, causal, nullptr, stream);
+}
+
+ATTN_API int attn_prefill_paged_qk_norm_rope(const void* Q, const void* k_cache, const void* v_cache,
+                                             void* O, const int* cu_seqlens_q,
+                                             const int* seq_lens_kv, const int* block_tables,
+                                             const void* q_weight, const float* cos_sin,
+                                             int max_pos, float eps, int B, int max_seqlen_q,
+                                             int total_q, int H_q, int H_kv, int D,
+                                             int max_blocks_per_seq, int block_size,
+                                             long long num_blocks, int causal, cudaStream_t stream)
+{
+    if (max_pos < 1 || !(eps >= 0.0f) || !std::isfinite(eps))
+        return ATTN_ERR_INVALID_ARG;
+    if (B > 0 && total_q > 0 && max_seqlen_q > 0) {
+        if (!cos_sin || !aligned(cos_sin, 16) || !aligned(q_weight, 16))
+            return ATTN_ERR_INVALID_ARG;
+        const size_t qbytes = (size_t)total_q * H_q * D * 2;
+        const size_t tbytes = (size_t)max_pos * D * sizeof(float);
+        if (overlap(O, qbytes, cos_sin, tbytes) || (q_weight && overlap(O, qbytes, q_weight, (size_t)D * 2)))
+            return ATTN_ERR_INVALID_ARG;
+    }
+    const attn::QueryPrologue qp{q_weight, cos_sin, max_pos, eps};
+    return prefill_paged_checked(Q, k_cache, v_cache, O, cu_seqlens_q, seq_lens_kv, block_tables, B,
+                                 max_seqlen_q, total_q, H_q, H_kv, D, max_blocks_per_seq,
+                                 block_size, num_blocks, causal, &qp, stream);
 }
 
 ATTN_API int attn_debug_prefill_stall(const void* Q, const void* K, const void* V, void* O, int B,
@@ -348,10 +383,11 @@ ATTN_API int attn_rope_cos_sin_table(float* cos_sin, int max_pos, int D, double 
 
 namespace {
 
-// Checks shared by both prologue entry points.
+// Checks shared by both prologue entry points.  Q may be null only where
+// `q_optional` (the keys-only form of the append).
 int validate_prologue(const void* Q, const void* K, const void* q_weight, const void* k_weight,
                       const float* cos_sin, int max_pos, const int* positions, int num_tokens,
-                      int H_q, int H_kv, int D, float eps)
+                      int H_q, int H_kv, int D, float eps, bool q_optional = false)
 {
     if (num_tokens < 0 || H_q < 1 || H_kv < 1 || max_pos < 1 || !(eps >= 0.0f) || !std::isfinite(eps))
         return ATTN_ERR_INVALID_ARG;
@@ -359,11 +395,11 @@ int validate_prologue(const void* Q, const void* K, const void* q_weight, const 
         return ATTN_ERR_UNSUPPORTED;
     if (num_tokens == 0)
         return ATTN_OK;
-    if (!Q || !K || !cos_sin || !positions || !aligned(Q, 16) || !aligned(K, 16) ||
+    if ((!Q && !q_optional) || !K || !cos_sin || !positions || !aligned(Q, 16) || !aligned(K, 16) ||
         !aligned(cos_sin, 16) || !aligned(positions, 4) || !aligned(q_weight, 16) ||
         !aligned(k_weight, 16))
         return ATTN_ERR_INVALID_ARG;
-    const size_t qb = (size_t)num_tokens * H_q * D * 2, kb = (size_t)num_tokens * H_kv * D * 2;
+    const size_t qb = Q ? (size_t)num_tokens * H_q * D * 2 : 0, kb = (size_t)num_tokens * H_kv * D * 2;
     const size_t tb = (size_t)max_pos * D / 2 * sizeof(float) * 2, pb = (size_t)num_tokens * 4;
     const void* read_only[] = {q_weight, k_weight, cos_sin, positions};
     const size_t ro_bytes[] = {(size_t)D * 2, (size_t)D * 2, tb, pb};
@@ -403,10 +439,10 @@ ATTN_API int attn_qk_norm_rope_append(void* Q, const void* K, const void* V, con
                                       float eps, cudaStream_t stream)
 {
     const int v = validate_prologue(Q, K, q_weight, k_weight, cos_sin, max_pos, positions,
-                                    num_tokens, H_q, H_kv, D, eps);
+                                    num_tokens, H_q, H_kv, D, eps, true);
     if (v != ATTN_OK)
         return v;
-    if (block_size != attn::kPageSize || H_q + 2 * H_kv > attn::kMaxPrologueRowsPerToken)
+    if (block_size != attn::kPageSize || (Q ? H_q : 0) + 2 * H_kv > attn::kMaxPrologueRowsPerToken)
         return ATTN_ERR_UNSUPPORTED;
     if (num_blocks < 0)
         return ATTN_ERR_INVALID_ARG;
@@ -415,7 +451,7 @@ ATTN_API int attn_qk_norm_rope_append(void* Q, const void* K, const void* V, con
     if (!V || !slot_mapping || !k_cache || !v_cache || !aligned(V, 16) || !aligned(slot_mapping, 8) ||
         !aligned(k_cache, 16) || !aligned(v_cache, 16))
         return ATTN_ERR_INVALID_ARG;
-    const size_t qb = (size_t)num_tokens * H_q * D * 2, kb = (size_t)num_tokens * H_kv * D * 2;
+    const size_t qb = Q ? (size_t)num_tokens * H_q * D * 2 : 0, kb = (size_t)num_tokens * H_kv * D * 2;
     const size_t cb = (size_t)num_blocks * H_kv * block_size * D * 2;
     if (overlap(Q, qb, V, kb) || overlap(k_cache, cb, v_cache, cb))
         return ATTN_ERR_INVALID_ARG;

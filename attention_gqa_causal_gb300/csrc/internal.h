@@ -76,15 +76,26 @@ int record_cuda_error(cudaError_t e);
 cudaError_t launch_prefill(const void* Q, const void* K, const void* V, void* O, int B, int S,
                            int H_q, int H_kv, int causal, int stall_tile, cudaStream_t stream);
 
+// The query prologue folded into the paged prefill: per-head RMSNorm weight
+// (nullptr = none), the cos/sin table of launch_rope_table with max_pos
+// positions, and eps.
+struct QueryPrologue {
+    const void* q_weight;
+    const float* cos_sin;
+    int max_pos;
+    float eps;
+};
+
 // Prefill of packed query chunks ([total_q, H_q, 128], cu_seqlens_q [B+1])
 // against a paged cache ([num_blocks, H_kv, 16, 128]) holding seq_lens_kv[b]
 // keys per sequence; query i of sequence b sits at position
-// seq_lens_kv[b] - L_q(b) + i.
+// seq_lens_kv[b] - L_q(b) + i.  With qp, each query row is first normalised
+// and rotated at that position (Q itself is only read).
 cudaError_t launch_prefill_paged(const void* Q, const void* k_cache, const void* v_cache, void* O,
                                  const int* cu_seqlens_q, const int* seq_lens_kv,
                                  const int* block_tables, int B, int max_seqlen_q, int total_q,
                                  int H_q, int H_kv, int max_blocks_per_seq, long long num_blocks,
-                                 int causal, cudaStream_t stream);
+                                 int causal, const QueryPrologue* qp, cudaStream_t stream);
 
 // The rotary table: per position 32 float4, entry p*32 + i*8 + m holding
 // {cos a, cos b, sin a, sin b} of the angles p * base^(-2j/128) of pairs
@@ -92,9 +103,9 @@ cudaError_t launch_prefill_paged(const void* Q, const void* k_cache, const void*
 cudaError_t launch_rope_table(float* cos_sin, int max_pos, double base, cudaStream_t stream);
 
 // Per-head RMSNorm (weights q_w / k_w, nullptr = none) then NeoX RoPE of q
-// [T, H_q, 128] (in place) and k [T, H_kv, 128].  Without k_cache, k goes to
-// k_out (may equal k); with k_cache, k and v go to the paged slots of
-// slot_mapping (-1 skipped) and k_out is unused.
+// [T, H_q, 128] (in place; q == nullptr: no query rows) and k [T, H_kv, 128].
+// Without k_cache, k goes to k_out (may equal k); with k_cache, k and v go to
+// the paged slots of slot_mapping (-1 skipped) and k_out is unused.
 cudaError_t launch_qk_norm_rope(void* q, const void* k, const void* v, void* k_out,
                                 const void* q_w, const void* k_w, const float* cos_sin,
                                 int max_pos, const int* positions, const long long* slot_mapping,

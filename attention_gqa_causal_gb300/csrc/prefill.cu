@@ -59,6 +59,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -114,6 +115,14 @@ struct PrefillArgs {
     const int* block_tables;  // [B, max_blocks]
     int max_blocks;
     int total_q;              // rows of packed Q / O
+    // paged form with the query prologue folded in (rope != 0): each Q row is
+    // normalised (q_w, nullptr = no norm) and rotated at its position in shared
+    // memory before the first score GEMM
+    int rope;
+    const __half* q_w;        // [128] RMSNorm weight or nullptr
+    const float4* rope_table; // [max_pos, 32] float4, the cos/sin table of attn_rope_cos_sin_table
+    int max_pos;
+    float eps;
 };
 
 struct Unit {
@@ -195,6 +204,7 @@ __device__ __forceinline__ Unit decode_unit(const PrefillArgs& a, int u)
 
 struct SmemCtl {
     uint64_t q_full;
+    uint64_t q_ready[2];     // tile t's rows normalised and rotated (query prologue folded in; 128 arrivals)
     uint64_t k_full[kKStages], k_empty[kKStages];
     uint64_t v_full[kVStages], v_empty[kVStages];
     uint64_t s_full[2], p_full[2], o_full[2];
@@ -207,9 +217,13 @@ struct SmemCtl {
 // Dynamic shared memory: the 1024-aligned tiles, then the control block.  The
 // whole 227 KB is requested; the alignment padding the layout can absorb is
 // what is left over (the kernel checks it at run time).
+// After it, the query prologue's RMSNorm weight row (256 bytes, bulk-copied
+// with the Q tiles).
 constexpr uint32_t kSmemAlloc = kSmemMax;
-constexpr uint32_t kAlignSlack = kSmemMax - kSmemBytes - (uint32_t)sizeof(SmemCtl);
-static_assert(kSmemBytes + sizeof(SmemCtl) <= kSmemMax, "shared memory layout too large");
+constexpr uint32_t kSmemW = (kSmemBytes + (uint32_t)sizeof(SmemCtl) + 127u) & ~127u;
+constexpr uint32_t kSmemEnd = kSmemW + D * 2;
+constexpr uint32_t kAlignSlack = kSmemMax - kSmemEnd;
+static_assert(kSmemEnd <= kSmemMax, "shared memory layout too large");
 
 template <int N>
 __device__ __forceinline__ void regs_increase()
@@ -241,6 +255,133 @@ __device__ __forceinline__ float max32(const uint32_t (&r)[32])
                      fmaxf(__uint_as_float(r[b + 6]), __uint_as_float(r[b + 7])));
     }
     return fmaxf(fmax3(m[0], m[1], m[2]), m[3]);
+}
+
+// Per-head QK-norm then NeoX RoPE of Q rows, in place in the Q tiles, by the
+// softmax warpgroups.  The arithmetic is the prologue's ("GRPO-CUDA Project
+// Memory" page, "Qwen3-Specific Notes" and "RoPE design"): y = w x /
+// sqrt(mean(x^2) + eps) in FP32 (no norm when w is null), then
+// out_i = y_i c - y_{i+64} s, out_{i+64} = y_{i+64} c + y_i s with (c, s) of
+// pair i at the row's position, rounded once to FP16.
+// Work split: 8 lanes per row, 4 rows per warp at a time.  Lane m of a group
+// owns the row's chunk m of both halves (elements 8m.. and their partners
+// 64+8m..), which in a tile's 128-byte-swizzled boxes sit at ((m ^ row % 8) <<
+// 4) of box 0 and box 1: no lane needs another's values except for the sum of
+// squares (a 3-step xor reduction).  The lane's cos/sin entries of a row are
+// entries i*8 + m (i < 4) of the table row, so a group reads 128 contiguous
+// bytes per load.  When the two tiles are two heads over the same rows, a row
+// index has one position in both, so each table row is fetched once: warpgroup
+// t takes rows [64t, 64t + 64) of both tiles (4 passes); otherwise warpgroup t
+// takes all 128 rows of its own tile (8 passes).
+// Mixed-precision FMA (sm_100+): d = a * b + c with FP16 a, b and FP32 c, d;
+// the product of two halves is exact in FP32, so no conversion is needed.
+__device__ __forceinline__ float fma_hhf(uint16_t a, uint16_t b, float c)
+{
+    float d;
+    asm("fma.rn.f32.f16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
+    return d;
+}
+
+// FP16 -> FP32 (exact) as an addition of +0 on the FMA path.
+__device__ __forceinline__ float h2f(uint16_t a)
+{
+    float d;
+    asm("add.rn.f32.f16 %0, %1, %2;" : "=f"(d) : "h"(a), "f"(0.f));
+    return d;
+}
+
+__device__ __forceinline__ uint16_t half_bits(const uint4& u, int e)
+{
+    const uint32_t w = e < 2 ? u.x : e < 4 ? u.y : e < 6 ? u.z : u.w;
+    return static_cast<uint16_t>((e & 1) ? w >> 16 : w & 0xffffu);
+}
+
+// One batch of N rows of this lane (row n of tile tile[n], table entries of
+// pass pass[n]): all loads first, then the sums of squares and their group
+// reductions interleaved over the rows, then the rotations and the stores (bit
+// n of `store`), so that the rows' latencies overlap.  The halves enter the
+// FP32 arithmetic through mixed-precision FMAs (x*x for the sum of squares,
+// x*w, exact, before the 1/rms factor), which avoids the narrow FP16->FP32
+// conversion path; each output is rounded once to FP16.
+template <int N, int P>
+__device__ __forceinline__ void norm_rope_batch(uint8_t* q_tiles, const int (&row)[N], const int (&tile)[N],
+                                                const int (&pass)[N], const float4 (&cs)[P][4],
+                                                uint32_t store, const uint4& w_lo, const uint4& w_hi,
+                                                bool norm, float eps, int lane)
+{
+    const int m = lane % 8;
+    const unsigned mask = 0xffu << (lane & 24);
+    uint32_t off_lo[N];
+    uint4 xl[N], xh[N];
+#pragma unroll
+    for (int n = 0; n < N; ++n) {
+        off_lo[n] = tile[n] * kTileBytes + row[n] * 128 + ((m ^ (row[n] % 8)) << 4);
+        xl[n] = *reinterpret_cast<const uint4*>(q_tiles + off_lo[n]);
+        xh[n] = *reinterpret_cast<const uint4*>(q_tiles + off_lo[n] + kBoxBytes);
+    }
+    float ss[N];
+    if (norm) {
+#pragma unroll
+        for (int n = 0; n < N; ++n) {
+            float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;   // short independent chains
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+                s0 = fma_hhf(half_bits(xl[n], e), half_bits(xl[n], e), s0);
+                s1 = fma_hhf(half_bits(xl[n], e + 1), half_bits(xl[n], e + 1), s1);
+                s2 = fma_hhf(half_bits(xh[n], e), half_bits(xh[n], e), s2);
+                s3 = fma_hhf(half_bits(xh[n], e + 1), half_bits(xh[n], e + 1), s3);
+            }
+            ss[n] = (s0 + s1) + (s2 + s3);
+        }
+#pragma unroll
+        for (int o = 4; o > 0; o >>= 1)
+#pragma unroll
+            for (int n = 0; n < N; ++n)
+                ss[n] += __shfl_xor_sync(mask, ss[n], o);
+    }
+#pragma unroll
+    for (int n = 0; n < N; ++n) {
+        float lo[8], hi[8];
+        if (norm) {
+            const float inv = rsqrtf(ss[n] * (1.0f / D) + eps);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                lo[e] = fma_hhf(half_bits(xl[n], e), half_bits(w_lo, e), 0.f) * inv;
+                hi[e] = fma_hhf(half_bits(xh[n], e), half_bits(w_hi, e), 0.f) * inv;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                lo[e] = h2f(half_bits(xl[n], e));
+                hi[e] = h2f(half_bits(xh[n], e));
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float4 t = cs[pass[n]][i];   // {cos a, cos b, sin a, sin b}, pairs a = 8m + 2i, b = a + 1
+            const float la = lo[2 * i], lb = lo[2 * i + 1], ha = hi[2 * i], hb = hi[2 * i + 1];
+            lo[2 * i] = fmaf(la, t.x, -ha * t.z);
+            lo[2 * i + 1] = fmaf(lb, t.y, -hb * t.w);
+            hi[2 * i] = fmaf(ha, t.x, la * t.z);
+            hi[2 * i + 1] = fmaf(hb, t.y, lb * t.w);
+        }
+        if (store >> n & 1u) {
+            uint4 olo, ohi;
+            olo.x = pack_half2(lo[0], lo[1]); olo.y = pack_half2(lo[2], lo[3]);
+            olo.z = pack_half2(lo[4], lo[5]); olo.w = pack_half2(lo[6], lo[7]);
+            ohi.x = pack_half2(hi[0], hi[1]); ohi.y = pack_half2(hi[2], hi[3]);
+            ohi.z = pack_half2(hi[4], hi[5]); ohi.w = pack_half2(hi[6], hi[7]);
+            *reinterpret_cast<uint4*>(q_tiles + off_lo[n]) = olo;
+            *reinterpret_cast<uint4*>(q_tiles + off_lo[n] + kBoxBytes) = ohi;
+        }
+    }
+}
+
+// Row of pass p for this lane: shared rows (both tiles, warpgroup t's half) or
+// the own tile's 128 rows.
+__device__ __forceinline__ int rope_row(bool shared, int t, int p, int quad, int lane)
+{
+    return (shared ? 64 * t : 0) + p * 16 + quad * 4 + lane / 8;
 }
 
 // P = exp2(S*c - m) for 32 columns, packed in place (column pair -> even slot);
@@ -297,6 +438,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             mbar_init(smem_u32(&ctl.v_empty[s]), 1);
         }
         for (int t = 0; t < 2; ++t) {
+            // 256 arrivals when both warpgroups rotate rows of both tiles (head pairs)
+            mbar_init(smem_u32(&ctl.q_ready[t]), a.head_pairs ? 256 : 128);
             mbar_init(smem_u32(&ctl.s_full[t]), 1);
             // tile 0's P barrier also takes the relay warp's arrival (operands in place)
             mbar_init(smem_u32(&ctl.p_full[t]), t == 0 ? 129 : 128);
@@ -326,7 +469,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 tma_prefetch_desc(&tmV);
                 tma_prefetch_desc(&tmO);
                 const uint32_t qbar = smem_u32(&ctl.q_full);
-                mbar_arrive_expect_tx(qbar, 2 * kTileBytes);
+                const bool q_weight = PAGED && a.rope && a.q_w;
+                mbar_arrive_expect_tx(qbar, 2 * kTileBytes + (q_weight ? D * 2 : 0));
+                if (q_weight)
+                    bulk_load(sbase + kSmemW, a.q_w, D * 2, qbar);
                 for (int t = 0; t < 2; ++t)
                     for (int h = 0; h < 2; ++h) {
                         const uint32_t dst = sbase + kSmemQ + t * kTileBytes + h * kBoxBytes;
@@ -458,12 +604,22 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     return true;
                 return __all_sync(0xffffffffu, mbar_wait(b, parity, abort)) != 0;
             };
-            bool ok = wait(ctl.q_full, 0) && wait(ctl.k_full[0], 0);
+            // with the query prologue folded in, each tile's score GEMM waits for its
+            // rows to be normalised and rotated (else for its TMA load)
+            const bool rope = PAGED && a.rope;
+            bool ok = wait(rope ? ctl.q_ready[0] : ctl.q_full, 0) && wait(ctl.k_full[0], 0);
             if (ok) {
                 tc_fence_after();
                 if (leader) {
                     issue_s(0, 0);
                     mma_commit(smem_u32(&ctl.s_full[0]));
+                }
+                __syncwarp();
+            }
+            ok = ok && (!rope || wait(ctl.q_ready[1], 0));
+            if (ok) {
+                tc_fence_after();
+                if (leader) {
                     issue_s(1, 0);
                     mma_commit(smem_u32(&ctl.s_full[1]));
                     mma_commit(smem_u32(&ctl.k_empty[0]));
@@ -557,6 +713,81 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         float m_ref = -CUDART_INF_F;  // reference max (log2 units) shared by l and O
         float l_sum = 0.f;
         bool ok = true;
+        if (PAGED && a.rope) {
+            // Query prologue (norm_rope_one).  Rows past the chunk are left as
+            // loaded (their output is not stored); a row whose position lies
+            // outside the table is left unrotated and flagged.  The table entries
+            // are fetched while the tiles are still in flight.
+            const bool norm = a.q_w != nullptr;
+            auto run = [&](auto shared_tag) -> bool {
+                constexpr bool kShared = decltype(shared_tag)::value;   // the tiles' rows share positions
+                constexpr int kPasses = kShared ? 4 : 8;
+                float4 cs[kPasses][4];
+                uint32_t rotate = 0;   // bit p (+ 8 for tile 1 when shared): rotate this lane's row of pass p
+                bool bad_pos = false;
+#pragma unroll
+                for (int p = 0; p < kPasses; ++p) {
+                    const int r = rope_row(kShared, t, p, quad, lane);
+#pragma unroll
+                    for (int tt = 0; tt < 2; ++tt) {
+                        if (kShared || tt == t) {
+                            const int qr_row = w.row0[tt] + r;
+                            const int pos = w.off + qr_row;
+                            if (qr_row < w.Lq) {
+                                if (pos >= 0 && pos < a.max_pos)
+                                    rotate |= 1u << (p + 8 * tt);
+                                else
+                                    bad_pos = true;
+                            }
+                        }
+                    }
+                    const int pos = w.off + (kShared ? w.row0[0] : my_row0) + r;
+                    const bool in_table = pos >= 0 && pos < a.max_pos;
+                    const float4* trow = a.rope_table + (size_t)(in_table ? pos : 0) * 32 + lane % 8;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        cs[p][i] = __ldg(trow + i * 8);
+                }
+                if (__any_sync(0xffffffffu, bad_pos) && lane == 0)
+                    atomicOr(a.err, kDevErrBadPosition);
+                if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.q_full), 0, abort)))
+                    return false;
+                uint4 wlo = make_uint4(0u, 0u, 0u, 0u), whi = wlo;
+                if (norm) {
+                    const uint4* wsm = reinterpret_cast<const uint4*>(smem + kSmemW);
+                    wlo = wsm[lane % 8];
+                    whi = wsm[8 + lane % 8];
+                }
+                // batches of rows per lane: shared, 2 passes x both tiles; own tile,
+                // 2 passes (its 8 passes' table entries already hold 128 registers)
+                constexpr int kBatch = kShared ? 4 : 2;
+#pragma unroll
+                for (int b = 0; b < 8 / kBatch; ++b) {   // 8 rows per lane either way
+                    int row[kBatch], tile[kBatch], pass[kBatch];
+                    uint32_t store = 0;
+#pragma unroll
+                    for (int n = 0; n < kBatch; ++n) {
+                        pass[n] = kShared ? 2 * b + n / 2 : kBatch * b + n;
+                        tile[n] = kShared ? n % 2 : t;
+                        row[n] = rope_row(kShared, t, pass[n], quad, lane);
+                        store |= (rotate >> (pass[n] + 8 * tile[n]) & 1u) << n;
+                    }
+                    norm_rope_batch(smem + kSmemQ, row, tile, pass, cs, store, wlo, whi, norm, a.eps, lane);
+                }
+                return true;
+            };
+            const bool shared = a.head_pairs;
+            if (shared ? run(std::true_type{}) : run(std::false_type{})) {
+                fence_proxy_async_smem();   // the score GEMMs read these rows through the async proxy
+                // both tiles' barriers when the rows are shared, else the own tile's
+                if (shared || t == 0)
+                    mbar_arrive(smem_u32(&ctl.q_ready[0]));
+                if (shared || t == 1)
+                    mbar_arrive(smem_u32(&ctl.q_ready[1]));
+            } else {
+                flag_abort(&ctl, a.err);   // every wait below now gives up at once
+            }
+        }
         for (int j = 0; j < w.n_kv; ++j) {
             ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.s_full[t]), j & 1, abort));
             if (!ok)
@@ -862,7 +1093,7 @@ cudaError_t launch_prefill_paged(const void* Q, const void* k_cache, const void*
                                  const int* cu_seqlens_q, const int* seq_lens_kv,
                                  const int* block_tables, int B, int max_seqlen_q, int total_q,
                                  int H_q, int H_kv, int max_blocks_per_seq, long long num_blocks,
-                                 int causal, cudaStream_t stream)
+                                 int causal, const QueryPrologue* qp, cudaStream_t stream)
 {
     cudaError_t e = ensure_smem_attr<true>();
     if (e != cudaSuccess)
@@ -883,6 +1114,13 @@ cudaError_t launch_prefill_paged(const void* Q, const void* k_cache, const void*
     a.block_tables = block_tables;
     a.max_blocks = max_blocks_per_seq;
     a.total_q = total_q;
+    if (qp) {
+        a.rope = 1;
+        a.q_w = static_cast<const __half*>(qp->q_weight);
+        a.rope_table = reinterpret_cast<const float4*>(qp->cos_sin);
+        a.max_pos = qp->max_pos;
+        a.eps = qp->eps;
+    }
     const long long grid = (long long)a.units_per_mb * a.n_mb;
     if (grid > 0x7fffffffLL)
         return cudaErrorInvalidConfiguration;

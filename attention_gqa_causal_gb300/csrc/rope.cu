@@ -195,7 +195,8 @@ __device__ __forceinline__ void producer(const PrologueArgs& a, unsigned char* s
         const uint32_t bar = smem_u32(full + s);
         const uint32_t dst = smem_u32(smem + s * a.stage_bytes);
         mbar_expect_tx(bar, (uint32_t)cn * a.R * kRowBytes);
-        bulk_load(dst, a.q + (size_t)t0 * a.H_q * kD, (uint32_t)cn * a.H_q * kRowBytes, bar);
+        if (a.H_q)
+            bulk_load(dst, a.q + (size_t)t0 * a.H_q * kD, (uint32_t)cn * a.H_q * kRowBytes, bar);
         bulk_load(dst + L.k_off, a.k + (size_t)t0 * a.H_kv * kD, (uint32_t)cn * a.H_kv * kRowBytes,
                   bar);
         if (APPEND)
@@ -458,6 +459,8 @@ cudaError_t launch_qk_norm_rope(void* q, const void* k, const void* v, void* k_o
 {
     PrologueArgs a;
     const bool append = k_cache != nullptr;
+    if (!q)
+        H_q = 0;   // keys (and values) only: the queries are normalised and rotated elsewhere
     a.q = static_cast<__half*>(q);
     a.k = static_cast<const __half*>(k);
     a.v = static_cast<const __half*>(v);

@@ -9,6 +9,9 @@ One step is one pass over every hot-path kernel on its workload:
     (L2 flushed before each launch: its inputs would otherwise stay in L2)
   * chunked prefill from the paged cache: 4 sequences, 6144 cached + 2048 new
     tokens each, H 32/8 (FLOPs over each query's visible keys)
+  * the same chunked step from raw projections, with its QK-norm + RoPE + KV
+    append prologue, unfused (separate query pass) and fused (queries
+    normalised and rotated inside the prefill kernel)
   * paged decode          256 sequences, lengths uniform on [128, 2048], H 16/8
   * paged decode          8 sequences x 32768 tokens, H 16/8
   * the 256-sequence decode step together with its KV append (two launches)
@@ -242,6 +245,41 @@ def build_legs(torch, ag, which):
                       "H_q": cfg.H_q, "H_kv": cfg.H_kv, "D": cfg.D, "causal": cfg.causal,
                       "block_size": 16, "num_blocks": int(kc.shape[0])}
         legs.append(leg)
+    if which in ("all", "layer"):
+        # One layer's attention step on the chunked workload, from raw projections:
+        # QK-norm + RoPE + KV append of the 4 x 2048 new tokens, then the chunked
+        # prefill.  Unfused: the prologue rewrites q in place and the prefill reads
+        # it back.  Fused: the prologue handles keys and values only and the
+        # prefill normalises and rotates each query row as it loads it.  Both are
+        # timed over their two launches, as TFLOP/s of the attention FLOPs.
+        cfg = W.CHUNKED_PREFILL
+        L = W.chunked_layer_inputs(cfg, seed=0)
+        cs = torch.empty((L["max_pos"], cfg.D), dtype=torch.float32, device="cuda")
+        ag.attn_rope_cos_sin_table(cs, W.PROLOGUE.base)
+        keys = ["Q", "k_cache", "v_cache", "cu_seqlens_q", "seq_lens_kv", "block_tables", "K", "V",
+                "q_weight", "k_weight", "positions", "slot_mapping"]
+        t = tuple(torch.from_numpy(L[k]).cuda() for k in keys)
+        Op = torch.empty_like(t[0])
+        for fused in (False, True):
+            name = f"layer_{cfg.name}_{'fused' if fused else 'unfused'}"
+            leg = Leg(name, "prefill", cfg.flops(), "TFLOP/s", 2)
+
+            def bind(t, o, fused=fused, c=cfg, cs=cs):
+                if fused:
+                    return lambda: (ag.attn_qk_norm_rope_append(
+                        None, t[6], t[7], None, t[9], cs, t[10], t[11], t[1], t[2], eps=1e-6, H_q=c.H_q),
+                        ag.attn_prefill_paged_qk_norm_rope(t[0], t[1], t[2], o, t[3], t[4], t[5], t[8], cs,
+                                                           c.chunk, eps=1e-6, causal=c.causal))
+                return lambda: (ag.attn_qk_norm_rope_append(
+                    t[0], t[6], t[7], t[8], t[9], cs, t[10], t[11], t[1], t[2], eps=1e-6),
+                    ag.attn_prefill_paged(t[0], t[1], t[2], o, t[3], t[4], t[5], c.chunk, causal=c.causal))
+            leg.set_buffers(bind, t, Op)
+            leg.host = {k: L[k] for k in keys}
+            leg.config = {"num_seqs": cfg.num_seqs, "prefix": cfg.prefix, "chunk": cfg.chunk,
+                          "H_q": cfg.H_q, "H_kv": cfg.H_kv, "D": cfg.D, "causal": cfg.causal,
+                          "rope_base": W.PROLOGUE.base, "eps": 1e-6,
+                          "query_prologue": "inside the prefill kernel" if fused else "separate pass"}
+            legs.append(leg)
     for cfg, key in ((W.DECODE_MIX, "decode"), (W.DECODE_LONG, "decode_long")):
         if which not in ("all", key) and not (key == "decode" and which == "decode_append"):
             continue
@@ -598,8 +636,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["all", "prefill", "prefill_full", "prefill_paged", "prologue", "qwen", "decode",
-                                           "decode_long", "decode_append"],
+    ap.add_argument("--workload", choices=["all", "prefill", "prefill_full", "prefill_paged", "layer", "prologue", "qwen",
+                                           "decode", "decode_long", "decode_append"],
                     default="all")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="CPU time budget of the oracle baseline sample")

@@ -88,6 +88,33 @@ ATTN_API int attn_prefill_paged(const void* Q, const void* k_cache, const void* 
                                 long long num_blocks, int causal, cudaStream_t stream);
 
 /*
+ * attn_prefill_paged with the query side of the attention-input prologue
+ * folded into the kernel's Q load ("GRPO-CUDA Project Memory" page, "Model
+ * forward pass": QK-norm -> RoPE -> KV append -> attention; "Qwen3-Specific
+ * Notes" and "RoPE design" for the per-head RMSNorm and the split-half
+ * rotation).  Q holds the raw query projections and is only read: query i of
+ * sequence b is first normalised, y = w * x / sqrt(mean(x^2) + eps) (no norm
+ * when q_weight is NULL), and rotated at its position L_kv - L_q + i with the
+ * table of attn_rope_cos_sin_table (max_pos positions), in FP32 rounded once
+ * to FP16 (attn_qk_norm_rope's definition; here x*w is formed exactly before
+ * the 1/rms factor, so a value may differ from that call's by one FP16 ulp),
+ * and then attends exactly as in attn_prefill_paged.  The cache must already hold normalised and
+ * rotated keys (attn_qk_norm_rope_append with Q = NULL writes them).
+ * q_weight : [D] FP16 or NULL (16-byte aligned); cos_sin : [max_pos, D] FP32
+ * (16-byte aligned); eps >= 0.  A query whose position lies outside
+ * [0, max_pos) is left unrotated and flagged (bit 128, ATTN_ERR_BAD_INPUT).
+ * Everything else as attn_prefill_paged.  One launch.
+ */
+ATTN_API int attn_prefill_paged_qk_norm_rope(const void* Q, const void* k_cache, const void* v_cache,
+                                             void* O, const int* cu_seqlens_q,
+                                             const int* seq_lens_kv, const int* block_tables,
+                                             const void* q_weight, const float* cos_sin,
+                                             int max_pos, float eps, int B, int max_seqlen_q,
+                                             int total_q, int H_q, int H_kv, int D,
+                                             int max_blocks_per_seq, int block_size,
+                                             long long num_blocks, int causal, cudaStream_t stream);
+
+/*
  * Failure-detection test hook (not for production use): attn_prefill, except
  * that the K tile with index stall_tile (>= 0) is never loaded in any CTA
  * that reaches it.  The on-chip waits for that tile run out after their
@@ -264,8 +291,11 @@ ATTN_API int attn_qk_norm_rope(void* Q, void* K, const void* q_weight, const voi
  * rotated in place as in attn_qk_norm_rope; K is normalised and rotated and V
  * copied straight into their paged cache slots (attn_kv_append's slot rules:
  * slot -1 skipped, out-of-range flagged with bit 32); K and V themselves are
- * only read.  Caches [num_blocks, H_kv, block_size, D] FP16, block_size 16,
- * must not overlap any input; H_q + 2*H_kv at most 192.  One launch.
+ * only read.  Q may be NULL: then only keys and values are processed (the
+ * queries' part runs inside attn_prefill_paged_qk_norm_rope) and H_q is not
+ * used beyond its check.  Caches [num_blocks, H_kv, block_size, D] FP16,
+ * block_size 16, must not overlap any input; H_q (0 when Q is NULL) + 2*H_kv
+ * at most 192.  One launch.
  */
 ATTN_API int attn_qk_norm_rope_append(void* Q, const void* K, const void* V, const void* q_weight,
                                       const void* k_weight, const float* cos_sin, int max_pos,

@@ -230,3 +230,45 @@ def test_qk_norm_rope_append_validation():
     assert qa(vc=A16 + 0x10000) == ag.ATTN_ERR_INVALID_ARG        # cache over the cos/sin table
     assert qa(Q=A16B + 0x4000000, Hq=180, Hkv=7) == ag.ATTN_ERR_UNSUPPORTED   # 194 rows per token
     assert qa(T=0) == ag.ATTN_OK
+
+
+def test_qk_norm_rope_append_keys_only_validation():
+    # Q = NULL: keys and values only; the row limit then counts 2 * H_kv alone
+    lib = ag.load()
+    F, LL = ctypes.c_float, ctypes.c_longlong
+
+    def qa(Q=0, K=A16 + 0x4000, V=A16 + 0x6000, T=4, Hq=8, Hkv=4, nb=16, eps=1e-6):
+        return lib.attn_qk_norm_rope_append(
+            P(Q), P(K), P(V), P(A16 + 0x8000), P(A16 + 0x8100), P(A16 + 0x10000), 64, P(A16 + 0x20000),
+            P(A16 + 0x20100), P(A16B), P(A16B + 0x1000000), T, Hq, Hkv, 128, 16, LL(nb), F(eps), P(0))
+
+    assert qa(K=0) == ag.ATTN_ERR_INVALID_ARG
+    assert qa(Hq=0) == ag.ATTN_ERR_INVALID_ARG
+    assert qa(Hq=97, Hkv=97, K=A16B + 0x4000000, V=A16B + 0x5000000) == ag.ATTN_ERR_UNSUPPORTED  # 194 rows
+    assert qa(T=0) == ag.ATTN_OK
+
+
+def test_prefill_paged_qk_norm_rope_validation():
+    lib = ag.load()
+    F, LL = ctypes.c_float, ctypes.c_longlong
+
+    def pr(Q=A16, kc=A16B, vc=A16B + 0x1000000, O=A16 + 0x100000, cu=A16 + 0x200000,
+           sl=A16 + 0x200100, bt=A16 + 0x200200, qw=A16 + 0x300000, cs=A16 + 0x400000, mp=4096,
+           eps=1e-6, B=2, mq=64, tq=100, Hq=4, Hkv=2, D=128, mb=8, bs=16, nb=16, causal=1):
+        return lib.attn_prefill_paged_qk_norm_rope(
+            P(Q), P(kc), P(vc), P(O), P(cu), P(sl), P(bt), P(qw), P(cs), mp, F(eps), B, mq, tq, Hq, Hkv,
+            D, mb, bs, LL(nb), causal, P(0))
+
+    assert pr(D=64) == ag.ATTN_ERR_UNSUPPORTED
+    assert pr(bs=32) == ag.ATTN_ERR_UNSUPPORTED
+    assert pr(mp=0) == ag.ATTN_ERR_INVALID_ARG
+    assert pr(eps=-1.0) == ag.ATTN_ERR_INVALID_ARG
+    assert pr(eps=float("inf")) == ag.ATTN_ERR_INVALID_ARG
+    assert pr(cs=0) == ag.ATTN_ERR_INVALID_ARG
+    assert pr(cs=MIS) == ag.ATTN_ERR_INVALID_ARG                  # table must be 16-byte aligned
+    assert pr(qw=A16 + 0x300008) == ag.ATTN_ERR_INVALID_ARG       # weight must be 16-byte aligned
+    assert pr(O=A16 + 0x400000 - 0x1000) == ag.ATTN_ERR_INVALID_ARG   # O over the table
+    assert pr(O=A16 + 64) == ag.ATTN_ERR_INVALID_ARG              # O overlaps Q
+    assert pr(Hq=6, Hkv=4) == ag.ATTN_ERR_INVALID_ARG
+    assert pr(B=0) == ag.ATTN_OK and pr(tq=0) == ag.ATTN_OK
+    assert pr(B=0, qw=0) == ag.ATTN_OK                            # no norm weight is allowed

@@ -283,3 +283,24 @@ def prologue_inputs(cfg: PrologueConfig, seed: int = 0):
     num_blocks = (T + 15) // 16
     slots = permutation(seed, 15, num_blocks * 16)[:T].astype(np.int64)
     return Q, K, V, qw, kw, positions, slots, num_blocks
+
+
+def chunked_layer_inputs(cfg: ChunkedPrefillConfig, seed: int = 0):
+    """One layer's attention step on the chunked workload, before its prologue:
+    the chunked-prefill inputs (Q as raw query projections; the caches hold the
+    cached prefixes), the chunk's own raw K and V rows [total_q, H_kv, D]
+    (streams 11/12), RMSNorm weights 1 + N(0,1)/4 (streams 13/14), each new
+    token's position (prefix .. prefix + chunk - 1) and its cache slot (the slot
+    of that position in its sequence's pages).  Returns a dict."""
+    Q, kc, vc, cu, lens_kv, tables = chunked_prefill_inputs(cfg, seed)
+    T = Q.shape[0]
+    K = normal_fp16(seed, 11, (T, cfg.H_kv, cfg.D))
+    V = normal_fp16(seed, 12, (T, cfg.H_kv, cfg.D))
+    qw = (1.0 + 0.25 * normal_fp16(seed, 13, (cfg.D,)).astype(np.float32)).astype(np.float16)
+    kw = (1.0 + 0.25 * normal_fp16(seed, 14, (cfg.D,)).astype(np.float32)).astype(np.float16)
+    pos = np.tile(np.arange(cfg.prefix, cfg.prefix + cfg.chunk, dtype=np.int32), cfg.num_seqs)
+    seq = np.repeat(np.arange(cfg.num_seqs), cfg.chunk)
+    slots = tables[seq, pos // 16].astype(np.int64) * 16 + pos % 16
+    return dict(Q=Q, k_cache=kc, v_cache=vc, cu_seqlens_q=cu, seq_lens_kv=lens_kv,
+                block_tables=tables, K=K, V=V, q_weight=qw, k_weight=kw, positions=pos,
+                slot_mapping=slots, max_pos=cfg.prefix + cfg.chunk)
