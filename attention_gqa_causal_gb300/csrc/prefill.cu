@@ -106,6 +106,7 @@ struct PrefillArgs {
     int head_pairs;     // 1: the two tiles are two heads; 0: two row tiles of one head
     int units_per_mb;   // B * H_kv * (tile pairs per kv head)
     int n_mb;           // number of row blocks (of the longest chunk when paged)
+    int groups_per_super;  // (batch, kv head) groups per super-group of the causal / paged order
     int causal;
     float scale_log2;   // log2(e) / sqrt(D)
     int stall_tile;     // failure-detection test only: key tile whose K load is withheld (-1: none)
@@ -146,10 +147,19 @@ __device__ __forceinline__ Unit decode_unit(const PrefillArgs& a, int u)
         r = u / a.n_mb;
         mb = u % a.n_mb;
     } else {
-        // causal (and paged): longest row blocks first so short ones fill the
+        // causal (and paged): the (batch, kv head) groups are taken a super-group
+        // at a time, so that the K/V the running CTAs read stays in L2 until
+        // every row block of its group has passed over it; inside a
+        // super-group longest row blocks come first, so short ones fill the
         // tail of the grid
-        mb = a.causal ? a.n_mb - 1 - u / a.units_per_mb : u / a.units_per_mb;
-        r = u % a.units_per_mb;
+        const int per_g = a.units_per_mb / (a.B * a.H_kv);
+        const int n_groups = a.B * a.H_kv;
+        const int units_per_super = a.n_mb * a.groups_per_super * per_g;
+        const int sup = u / units_per_super;
+        const int v = u - sup * units_per_super;
+        const int per_mb_here = min(a.groups_per_super, n_groups - sup * a.groups_per_super) * per_g;
+        mb = a.causal ? a.n_mb - 1 - v / per_mb_here : v / per_mb_here;
+        r = sup * a.groups_per_super * per_g + v % per_mb_here;
     }
     const int per_g = a.units_per_mb / (a.B * a.H_kv);
     const int pr = r % per_g;
@@ -1047,6 +1057,17 @@ cudaError_t ensure_smem_attr()
     return cudaSuccess;
 }
 
+// (batch, kv head) groups per super-group of the unit order: as many as keep
+// their K and V (2 * keys * 256 bytes each, keys bounded by max_keys) within
+// about a quarter of the 129 MB L2.
+int groups_per_super(int n_groups, long long max_keys)
+{
+    constexpr long long kBudget = 32ll << 20;
+    const long long per_group = 2 * max_keys * D * 2;
+    const long long g = per_group > 0 ? kBudget / per_group : n_groups;
+    return (int)(g < 1 ? 1 : (g > n_groups ? n_groups : g));
+}
+
 void fill_common(PrefillArgs& a, int B, int H_q, int H_kv, int rows, int causal)
 {
     a.B = B;
@@ -1057,6 +1078,7 @@ void fill_common(PrefillArgs& a, int B, int H_q, int H_kv, int rows, int causal)
     const int pairs_per_g = a.head_pairs ? a.group / 2 : a.group;
     a.n_mb = a.head_pairs ? (rows + BM - 1) / BM : (rows + 2 * BM - 1) / (2 * BM);
     a.units_per_mb = B * H_kv * pairs_per_g;
+    a.groups_per_super = B * H_kv;   // one super-group unless the caller sizes them
     a.causal = causal ? 1 : 0;
     a.scale_log2 = kLog2e / sqrtf((float)D);
     a.stall_tile = -1;
@@ -1080,6 +1102,7 @@ cudaError_t launch_prefill(const void* Q, const void* K, const void* V, void* O,
     if (!a.err)
         return cudaErrorInvalidSymbol;
     fill_common(a, B, H_q, H_kv, S, causal);
+    a.groups_per_super = groups_per_super(B * H_kv, (long long)S);
     a.S = S;
     a.stall_tile = stall_tile;
     const long long grid = (long long)a.units_per_mb * a.n_mb;
@@ -1108,6 +1131,7 @@ cudaError_t launch_prefill_paged(const void* Q, const void* k_cache, const void*
     if (!a.err)
         return cudaErrorInvalidSymbol;
     fill_common(a, B, H_q, H_kv, max_seqlen_q, causal);
+    a.groups_per_super = groups_per_super(B * H_kv, (long long)max_blocks_per_seq * kPageSize);
     a.S = 0;
     a.cu_q = cu_seqlens_q;
     a.seq_lens_kv = seq_lens_kv;
