@@ -7,11 +7,12 @@ One step is one pass over every hot-path kernel on its workload:
   * the same shape without the mask (the unmasked tensor-core ceiling)
   * causal GQA prefill at the Qwen3-0.6B attention shape, B=4, S=1024, H 16/8
     (L2 flushed before each launch: its inputs would otherwise stay in L2)
-  * chunked prefill from the paged cache: 4 sequences, 6144 cached + 2048 new
-    tokens each, H 32/8 (FLOPs over each query's visible keys)
-  * the same chunked step from raw projections, with its QK-norm + RoPE + KV
-    append prologue, unfused (separate query pass) and fused (queries
-    normalised and rotated inside the prefill kernel)
+  * one layer's chunked step from raw projections (4 sequences, 6144 cached +
+    2048 new tokens each, H 32/8), with its QK-norm + RoPE + KV append
+    prologue, unfused (separate query pass) and fused (queries normalised and
+    rotated inside the prefill kernel)
+  * the chunked prefill alone (FLOPs over each query's visible keys); it runs
+    just before the decode legs, as it leaves the least dirty data in L2
   * paged decode          256 sequences, lengths uniform on [128, 2048], H 16/8
   * paged decode          8 sequences x 32768 tokens, H 16/8
   * the 256-sequence decode step together with its KV append (two launches)
@@ -231,20 +232,6 @@ def build_legs(torch, ag, which):
             leg.config = {"B": cfg.B, "S": cfg.S, "H_q": cfg.H_q, "H_kv": cfg.H_kv, "D": cfg.D,
                           "causal": True, "l2": "flushed before each launch" if flush else "warm"}
             legs.append(leg)
-    if which in ("all", "prefill_paged"):
-        cfg = W.CHUNKED_PREFILL
-        Qp, kc, vc, cu, skv, tables = W.chunked_prefill_inputs(cfg, seed=0)
-        t = [torch.from_numpy(x).cuda() for x in (Qp, kc, vc, cu, skv, tables)]
-        Op = torch.empty_like(t[0])
-        leg = Leg(cfg.name, "prefill", cfg.flops(), "TFLOP/s", 1)
-        leg.set_buffers(lambda t, o, c=cfg: (lambda: ag.attn_prefill_paged(
-            t[0], t[1], t[2], o, t[3], t[4], t[5], c.chunk, causal=c.causal)), tuple(t), Op)
-        leg.host = {"Q": Qp, "k_cache": kc, "v_cache": vc, "cu_seqlens_q": cu, "seq_lens_kv": skv,
-                    "block_tables": tables}
-        leg.config = {"num_seqs": cfg.num_seqs, "prefix": cfg.prefix, "chunk": cfg.chunk,
-                      "H_q": cfg.H_q, "H_kv": cfg.H_kv, "D": cfg.D, "causal": cfg.causal,
-                      "block_size": 16, "num_blocks": int(kc.shape[0])}
-        legs.append(leg)
     if which in ("all", "layer"):
         # One layer's attention step on the chunked workload, from raw projections:
         # QK-norm + RoPE + KV append of the 4 x 2048 new tokens, then the chunked
@@ -280,6 +267,20 @@ def build_legs(torch, ag, which):
                           "rope_base": W.PROLOGUE.base, "eps": 1e-6,
                           "query_prologue": "inside the prefill kernel" if fused else "separate pass"}
             legs.append(leg)
+    if which in ("all", "prefill_paged"):
+        cfg = W.CHUNKED_PREFILL
+        Qp, kc, vc, cu, skv, tables = W.chunked_prefill_inputs(cfg, seed=0)
+        t = [torch.from_numpy(x).cuda() for x in (Qp, kc, vc, cu, skv, tables)]
+        Op = torch.empty_like(t[0])
+        leg = Leg(cfg.name, "prefill", cfg.flops(), "TFLOP/s", 1)
+        leg.set_buffers(lambda t, o, c=cfg: (lambda: ag.attn_prefill_paged(
+            t[0], t[1], t[2], o, t[3], t[4], t[5], c.chunk, causal=c.causal)), tuple(t), Op)
+        leg.host = {"Q": Qp, "k_cache": kc, "v_cache": vc, "cu_seqlens_q": cu, "seq_lens_kv": skv,
+                    "block_tables": tables}
+        leg.config = {"num_seqs": cfg.num_seqs, "prefix": cfg.prefix, "chunk": cfg.chunk,
+                      "H_q": cfg.H_q, "H_kv": cfg.H_kv, "D": cfg.D, "causal": cfg.causal,
+                      "block_size": 16, "num_blocks": int(kc.shape[0])}
+        legs.append(leg)
     for cfg, key in ((W.DECODE_MIX, "decode"), (W.DECODE_LONG, "decode_long")):
         if which not in ("all", key) and not (key == "decode" and which == "decode_append"):
             continue
