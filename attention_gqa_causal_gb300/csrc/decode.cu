@@ -28,6 +28,10 @@
 //    (O normalised, lse natural log) per head; the combine kernel merges the
 //    splits.  Empty splits (past the end of a sequence) exit at once and are
 //    skipped by the combine, which recomputes the split count from seq_lens.
+//  * The launches of a step (KV append, main kernel, combine) are chained by
+//    programmatic dependent launch: each kernel lets its dependent be
+//    scheduled as soon as its own CTAs have started, and the dependent waits on
+//    the device for its results, so the launch gaps overlap the tails.
 #include <cstdint>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -65,6 +69,21 @@ namespace {
 constexpr int kDecodeWarps = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+
+// Programmatic dependent launch (sm_90+): a kernel launched with programmatic
+// stream serialization may start before the previous kernel in the stream has
+// finished; it must wait (grid_dependency_wait) before touching what that
+// kernel writes.  A kernel lets its dependent start early with
+// allow_dependents.  Both are no-ops without such a dependency.
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void allow_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 __device__ __forceinline__ uint4 ld_stream16(const void* p)
 {
@@ -108,6 +127,8 @@ decode_splitk_kernel(const __half* __restrict__ q, const __half* __restrict__ k_
 {
     constexpr int D = kHeadDim;
     constexpr int BS = kPageSize;
+    grid_dependency_wait();   // the cache may have been written by the launch before (KV append)
+    allow_dependents();       // the combine may be scheduled once every CTA has started
     const int split = blockIdx.x % n_split;
     int rest = blockIdx.x / n_split;
     const int chunk = rest % chunks;
@@ -314,6 +335,7 @@ lse_combine_kernel(const float* __restrict__ O_part, const float* __restrict__ l
     __shared__ float sm_max[W];
     __shared__ float sm_sum[W];
     __shared__ float4 sm_acc[W][32];
+    grid_dependency_wait();   // the partials come from the launch before
     const int row = blockIdx.x;
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -450,6 +472,21 @@ size_t decode_workspace_bytes(const DecodePlan& p)
     return a + ((p.lse_part_bytes + 255) & ~size_t(255));
 }
 
+// Launch configuration of a kernel that may start while the previous kernel in
+// the stream finishes (it waits on the device before reading that kernel's output).
+static void dependent_launch(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr)[1], dim3 grid, dim3 block,
+                             cudaStream_t stream)
+{
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+}
+
 template <int GP>
 static cudaError_t launch_main(const DecodePlan& p, const void* q, const void* k_cache,
                                const void* v_cache, const int* block_tables, const int* seq_lens,
@@ -459,11 +496,13 @@ static cudaError_t launch_main(const DecodePlan& p, const void* q, const void* k
     if (grid > 0x7fffffffLL)
         return cudaErrorInvalidConfiguration;
     const float q_scale = kLog2e / sqrtf((float)kHeadDim);
-    decode_splitk_kernel<GP><<<(unsigned)grid, kDecodeWarps * 32, 0, stream>>>(
-        static_cast<const __half*>(q), static_cast<const __half*>(k_cache),
-        static_cast<const __half*>(v_cache), block_tables, seq_lens, O_part, lse_part, p.H_q,
-        p.H_kv, p.group, p.chunks, p.max_blocks_per_seq, p.pages_per_split, p.n_split, q_scale);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    dependent_launch(cfg, attr, dim3((unsigned)grid), dim3(kDecodeWarps * 32), stream);
+    return cudaLaunchKernelEx(&cfg, decode_splitk_kernel<GP>, static_cast<const __half*>(q),
+                              static_cast<const __half*>(k_cache), static_cast<const __half*>(v_cache),
+                              block_tables, seq_lens, O_part, lse_part, p.H_q, p.H_kv, p.group, p.chunks,
+                              p.max_blocks_per_seq, p.pages_per_split, p.n_split, q_scale);
 }
 
 cudaError_t launch_decode(const DecodePlan& p, const void* q, const void* k_cache,
@@ -483,10 +522,12 @@ cudaError_t launch_decode(const DecodePlan& p, const void* q, const void* k_cach
     if (e != cudaSuccess)
         return e;
     const int R = p.num_seqs * p.H_q;
-    lse_combine_kernel<<<R, kCombineWarps * 32, 0, stream>>>(
-        O_part, lse_part, static_cast<__half*>(out), p.n_split, seq_lens, p.H_q,
-        p.pages_per_split, p.max_blocks_per_seq * kPageSize);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    dependent_launch(cfg, attr, dim3((unsigned)R), dim3(kCombineWarps * 32), stream);
+    return cudaLaunchKernelEx(&cfg, lse_combine_kernel, (const float*)O_part, (const float*)lse_part,
+                              static_cast<__half*>(out), p.n_split, seq_lens, p.H_q, p.pages_per_split,
+                              p.max_blocks_per_seq * kPageSize);
 }
 
 cudaError_t launch_lse_combine(const float* O_part, const float* lse_part, void* out, int R,
@@ -513,6 +554,7 @@ kv_append_kernel(const __half* __restrict__ k_new, const __half* __restrict__ v_
 {
     constexpr int D = kHeadDim;
     constexpr int BS = kPageSize;
+    allow_dependents();
     const int t = blockIdx.x;
     const long long slot = slot_mapping[t];
     if (slot < 0 || slot >= num_blocks * BS) {
