@@ -228,3 +228,13 @@ def test_split_of_negative_block_ids_contributes_nothing(pps):
     ref = oracle.decode_paged(inp.q, inp.k_cache, inp.v_cache, ct, cl)
     assert np.all(out[1] == 0)
     assert_close(out, ref, f"negative-id split, pages_per_split={pps}")
+
+
+def test_many_sequences_short_contexts():
+    # 4096 sequences of 0..64 tokens: a grid of 8192 CTAs, most splits past the context
+    lens = W.uniform_int(79, 3, 4096, 0, 64)
+    inp = make(len(lens), 16, 8, lens, max_blocks=8, seed=79)
+    out = run_decode(inp)
+    assert np.all(out[np.asarray(lens) == 0] == 0)
+    assert_close(out, oracle_decode(inp), "4096 short sequences")
+    assert device_error_clean()

@@ -157,3 +157,26 @@ def test_wide_groups_and_many_heads(causal, heads):
     assert_close(run_prefill(Q, K, V, causal), oracle.prefill(Q, K, V, causal=causal),
                  f"S={S} causal={causal} heads={heads}")
     assert device_error_clean()
+
+
+def test_long_single_sequence_stratified():
+    # the largest sequence here: S 32768, one batch entry, H 8/1 (group 8: head pairs)
+    B, S, H_q, H_kv = 1, 32768, 8, 1
+    Q, K, V = rand_inputs(B, S, H_q, H_kv, seed=77)
+    O = torch.full(Q.shape, float("nan"), dtype=torch.float16, device="cuda")
+    ag.attn_prefill(dev(Q), dev(K), dev(V), O, causal=True)
+    torch.cuda.synchronize()
+    O = host(O)
+    assert np.isfinite(O.astype(np.float32)).all(), "rows left unwritten"
+    rows = stratified_rows(B, S, H_q, seed=4, diag_blocks=(0, S // 128 - 1), diag_heads=(0, H_q - 1))
+    ref = oracle.prefill_rows(Q, K, V, rows, causal=True)
+    assert_close(O[rows[:, 0], rows[:, 1], rows[:, 2]], ref, f"S={S}: {len(rows)} stratified rows")
+    assert device_error_clean()
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_many_tiny_batches(causal):
+    # 64 batch entries of 16 tokens: one ragged tile per CTA, 512 CTAs
+    Q, K, V = rand_inputs(64, 16, 16, 8, seed=78)
+    assert_close(run_prefill(Q, K, V, causal), oracle.prefill(Q, K, V, causal=causal), f"B=64 S=16 causal={causal}")
+    assert device_error_clean()

@@ -149,3 +149,15 @@ def test_wide_groups_and_many_heads(heads):
     out = run(Q, kc, vc, cu, skv, table)
     assert_close(out, oracle.prefill_paged(Q, kc, vc, cu, skv, table), f"paged prefill heads={heads}")
     assert device_error_clean()
+
+
+def test_one_long_chunk_without_prefix():
+    # a single 8192-token chunk with an empty cache prefix (the whole prompt at once)
+    rng = np.random.default_rng(67)
+    _, _, kc, vc, table, Q, cu, skv = _paged_problem(rng, [8192], [8192], 16, 8, 128, nan_unused=False)
+    out = run(Q, kc, vc, cu, skv, table)
+    assert np.isfinite(out.astype(np.float32)).all(), "rows left unwritten"
+    rows = stratified_rows(1, 8192, 16, seed=5, diag_blocks=(0, 63), diag_heads=(0, 15))
+    ref = oracle.prefill_paged_rows(Q, kc, vc, cu, skv, table, rows)
+    assert_close(out[cu[rows[:, 0]] + rows[:, 1], rows[:, 2]], ref, "one 8192-token chunk")
+    assert device_error_clean()
