@@ -39,11 +39,13 @@
 // row max exceeds it by more than kRescaleThreshold (log2 units); O and l
 // always refer to the same m, so the result is exact.  Because m rarely moves
 // after the first key tile, the exponentials of a tile are computed
-// optimistically against the current m while the tile's max is reduced
-// alongside; in the rare case that the max exceeds the threshold, the warp
-// reloads S (still intact in TMEM: P has not been written yet), moves m,
-// rescales O and recomputes.  This keeps the max reduction off the path from
-// "S ready" to "P ready" that the tensor core waits for.
+// optimistically against the current m, and in the common case the tile's max
+// is not reduced at all: every p of a row is at most the row's sum, so a sum
+// within 2^kRescaleThreshold proves that no p went past the threshold.  Only
+// when a row's sum exceeds it does the warp reload S (still intact in TMEM: P
+// has not been written yet), take the tile max, move m if it grew past the
+// threshold (rescaling O) and recompute.  This keeps the max reduction off the
+// path from "S ready" to "P ready" that the tensor core waits for.
 // TMEM: S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512) columns.
 // SMEM: Q0,Q1 (32 KB each), 2 K stages, 2 V stages (32 KB each), all
 // 128-byte swizzled as written by TMA boxes of 64 x 128 (contiguous K/V) or
@@ -96,6 +98,7 @@ constexpr uint32_t kSmemV = kSmemK + kKStages * kTileBytes;
 constexpr uint32_t kSmemBytes = kSmemV + kVStages * kTileBytes;
 constexpr uint32_t kSmemMax = 232448;               // 227 KB: the per-CTA opt-in limit
 constexpr float kRescaleThreshold = 8.0f;
+constexpr float kSumLimit = 256.0f;   // 2^kRescaleThreshold
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct PrefillArgs {
@@ -840,37 +843,40 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             load_s();
             if (j == 0)
                 move_ref(fmaxf(fmax3(max32(sr[0]), max32(sr[1]), max32(sr[2])), max32(sr[3])));
-            // One straight pass against the current reference, the tile max reduced
-            // alongside (on the first tile the reference is already the max).
+            // One straight pass against the current reference.  Every p of the row is
+            // at most the row's sum, so a sum within 2^threshold proves that no p
+            // exceeds it and the reference holds; only otherwise is the tile's max
+            // taken (from S, still intact in TMEM) to decide.
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-                rs[k] = 0.f;
-            float mx = -CUDART_INF_F;
+            for (int k8 = 0; k8 < 8; ++k8)
+                rs[k8] = 0.f;
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                mx = fmaxf(mx, max32(sr[q4]));
+            for (int q4 = 0; q4 < 4; ++q4)
                 exp_pack32(sr[q4], c, -m_ref, rs);
-            }
-            if (j > 0 && __any_sync(0xffffffffu, mx * c > m_ref + kRescaleThreshold)) {
-                // rare: the reference was too low for this tile.  S is still intact
-                // in TMEM (P has not been written): reload it, move the reference
-                // and redo the pass.
-                move_ref(mx);
+            fadd2(rs[0], rs[1], rs[2], rs[3]);
+            fadd2(rs[4], rs[5], rs[6], rs[7]);
+            fadd2(rs[0], rs[1], rs[4], rs[5]);
+            float tile_sum = rs[0] + rs[1];
+            if (j > 0 && __any_sync(0xffffffffu, tile_sum > kSumLimit)) {
+                // rare: reload S, move the reference if the max grew past the
+                // threshold, and redo the pass (the same values if it did not)
                 load_s();
+                move_ref(fmaxf(fmax3(max32(sr[0]), max32(sr[1]), max32(sr[2])), max32(sr[3])));
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    rs[k] = 0.f;
+                for (int k8 = 0; k8 < 8; ++k8)
+                    rs[k8] = 0.f;
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4)
                     exp_pack32(sr[q4], c, -m_ref, rs);
+                fadd2(rs[0], rs[1], rs[2], rs[3]);
+                fadd2(rs[4], rs[5], rs[6], rs[7]);
+                fadd2(rs[0], rs[1], rs[4], rs[5]);
+                tile_sum = rs[0] + rs[1];
             }
             // S has been read for the last time: P overwrites its first 64 columns
             tmem_st32_even(tS, sr[0], sr[1]);
             tmem_st32_even(tS + 32, sr[2], sr[3]);
-            fadd2(rs[0], rs[1], rs[2], rs[3]);
-            fadd2(rs[4], rs[5], rs[6], rs[7]);
-            fadd2(rs[0], rs[1], rs[4], rs[5]);
-            l_sum += rs[0] + rs[1];
+            l_sum += tile_sum;
             if (j > 0 && __any_sync(0xffffffffu, grow)) {
                 // O_t holds the previous tiles' sum (its last PV completed before
                 // s_full fired and the next PV waits for p_full): bring it to the
