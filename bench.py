@@ -143,8 +143,9 @@ def dram_traffic(kernel: str, workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clock and throttle reasons while running."""
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi sampling of SM clock and throttle reasons while running.  Rows carry
+    nvidia-smi's own timestamp, so stop() can keep those taken inside the timed region."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -152,12 +153,30 @@ class ClockSampler:
         self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
         try:
             self.p = subprocess.Popen(["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}",
-                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                       "--format=csv,noheader,nounits", "-lms", "20"],
                                       stdout=self.f, stderr=subprocess.DEVNULL)
         except OSError:
             self.p = None
 
-    def stop(self):
+    def wait_ready(self, timeout: float = 5.0):
+        """Block until the first sample is written (nvidia-smi takes a moment to start)."""
+        end = time.time() + timeout
+        while self.p is not None and time.time() < end and self.p.poll() is None:
+            if os.path.getsize(self.f.name) > 0:
+                return
+            time.sleep(0.01)
+
+    @staticmethod
+    def _epoch(stamp: str):
+        import datetime
+        try:
+            return datetime.datetime.strptime(stamp.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
+    def stop(self, window=None):
+        """Summarise the samples; with window = (t0, t1) in epoch seconds, only those
+        stamped inside it (all of them if none fall inside)."""
         if self.p is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.p.terminate()
@@ -165,19 +184,27 @@ class ClockSampler:
         self.f.seek(0)
         rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.strip()]
         os.unlink(self.f.name)
+        inside = rows
+        if window is not None:
+            t0, t1 = window
+            inside = [r for r in rows if (lambda t: t is not None and t0 <= t <= t1)(self._epoch(r[0]))]
+            if not inside:
+                inside = rows
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
+        for r in inside:
             try:
-                sm.append(float(r[0]))
-                mx = float(r[1])
-                for name, v in zip(names, r[4:8]):
+                sm.append(float(r[1]))
+                mx = float(r[2])
+                for name, v in zip(names, r[5:9]):
                     if v.strip().lower() == "active":
                         reasons.add(name)
             except (ValueError, IndexError):
                 continue
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "samples": len(sm), "reasons": sorted(reasons)}
+                "samples": len(sm), "samples_run": len(rows),
+                "window": "timed region" if inside is not rows else "whole run",
+                "reasons": sorted(reasons)}
 
 
 # ------------------------------------------------------------------ GPU legs
@@ -357,6 +384,7 @@ def time_device(torch, legs, steps, warmup, dist, use_cuda):
         dist.barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
+    time_device.window = (time.time(), None)
     for s in range(steps):
         for i, leg in enumerate(legs):
             if getattr(leg, "flush", False):
@@ -368,6 +396,7 @@ def time_device(torch, legs, steps, warmup, dist, use_cuda):
     if dist is not None:
         dist.barrier()
     wall = time.perf_counter() - t0
+    time_device.window = (time_device.window[0], time.time())
     for i, leg in enumerate(legs):
         leg.times = [ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(steps)]
     return wall
@@ -533,8 +562,9 @@ def run_ours(args):
     legs = build_legs(torch, ag, args.workload)
     torch.cuda.synchronize()
     clocks = ClockSampler(local)
+    clocks.wait_ready()
     wall = time_device(torch, legs, args.steps, args.warmup, dist, True)
-    clk = clocks.stop()
+    clk = clocks.stop(time_device.window)
     wall = reduce_max(dist, wall, True)
     err = ag.attn_get_device_error(reset=True)
     peaks, peak_src = load_peaks()

@@ -61,3 +61,39 @@ def test_reference_arm_prints_one_contract_line():
         assert key in d, key
     assert d["impl"] == "reference" and d["cpu_baseline"]["kind"] == "oracle"
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+
+
+def test_clock_summary_keeps_only_samples_inside_the_timed_region(tmp_path):
+    """The clocks line reports samples stamped inside the timed window, with their
+    throttle reasons; a window that no sample falls in falls back to the whole run."""
+    import datetime
+    import time as _time
+
+    class _Done:
+        def terminate(self):
+            pass
+
+        def wait(self):
+            pass
+
+    def sampler(rows):
+        c = bench.ClockSampler.__new__(bench.ClockSampler)
+        path = tmp_path / f"clk{len(rows)}_{_time.monotonic_ns()}.csv"
+        path.write_text("".join(rows))
+        c.f = open(path, "r+")
+        c.p = _Done()
+        return c
+
+    now = _time.time()
+    rows = []
+    for k, (mhz, cap) in enumerate([(1500, "Not Active"), (2070, "Not Active"),
+                                    (2040, "Not Active"), (1900, "Active")]):
+        stamp = datetime.datetime.fromtimestamp(now + 0.02 * k).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        rows.append(f"{stamp}, {mhz}, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, {cap}\n")
+    inside = sampler(rows).stop((now + 0.01, now + 0.05))
+    assert inside["samples"] == 2 and inside["samples_run"] == 4
+    assert inside["window"] == "timed region"
+    assert inside["sm_mhz"] == 2055.0 and inside["reasons"] == []
+    outside = sampler(rows).stop((now + 10.0, now + 11.0))
+    assert outside["window"] == "whole run" and outside["samples"] == 4
+    assert outside["reasons"] == ["sw_power_cap"]
