@@ -20,7 +20,8 @@
 //   warps 0-3  softmax of Q tile 0 (TMEM lanes 0..127 = its rows)
 //   warps 4-7  softmax of Q tile 1
 //   warp  8    MMA warp (one lane issues) + TMEM allocation
-//   warp  9    TMA producer (one lane)
+//   warp  9    TMA producer (one lane); it also initialises the barriers and
+//              sends the first Q/K/V copies before the set-up barrier
 //   warp 10    relay (one lane): adds "V_j and K_{j+1} landed" to tile 0's P
 //              barrier, so the MMA warp checks one barrier per step
 //   warp 11    idle (it completes the third warpgroup)
@@ -217,6 +218,7 @@ __device__ __forceinline__ Unit decode_unit(const PrefillArgs& a, int u)
 
 struct SmemCtl {
     uint64_t q_full;
+    uint64_t q0_full;        // Q tile 0 landed (without the query prologue; q_full then covers tile 1)
     uint64_t q_ready[2];     // tile t's rows normalised and rotated (query prologue folded in; 128 arrivals)
     uint64_t k_full[kKStages], k_empty[kKStages];
     uint64_t v_full[kVStages], v_empty[kVStages];
@@ -439,9 +441,48 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         return;  // uniform over the CTA, before any barrier or allocation
     volatile int* abort = &ctl.abort;
 
-    if (threadIdx.x == 0) {
+    const bool rope = PAGED && a.rope;
+    const int* const trow = PAGED ? a.block_tables + (size_t)w.b * a.max_blocks : nullptr;
+    // one K or V tile into `dst`: a 64 x 128 box per half (contiguous), or
+    // one 64 x 16 box per half and page (paged; a page past the context, or
+    // any id outside the cache, reads as zeros)
+    auto load_tile = [&](const CUtensorMap* map, uint32_t dst, uint32_t bar, int j) {
+        if (PAGED) {
+            int phys[kPagesPerTile];
+#pragma unroll
+            for (int k = 0; k < kPagesPerTile; ++k) {
+                const int p = j * kPagesPerTile + k;
+                phys[k] = p < w.n_pages ? trow[p] : -1;
+            }
+#pragma unroll
+            for (int k = 0; k < kPagesPerTile; ++k)
+                for (int h = 0; h < 2; ++h)
+                    tma_load_4d(dst + h * kBoxBytes + k * kPageBoxBytes, map, bar, h * 64, 0, w.g, phys[k]);
+        } else {
+            for (int h = 0; h < 2; ++h)
+                tma_load_4d(dst + h * kBoxBytes, map, bar, h * 64, w.g, j * BN, w.b);
+        }
+    };
+    auto load_q = [&](int t, uint32_t bar) {
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t dst = sbase + kSmemQ + t * kTileBytes + h * kBoxBytes;
+            if (PAGED)
+                tma_load_3d(dst, &tmQ, bar, h * 64, w.head[t], w.q_base + w.row0[t]);
+            else
+                tma_load_4d(dst, &tmQ, bar, h * 64, w.head[t], w.row0[t], w.b);
+        }
+    };
+
+    // The TMA thread sets up the barriers and sends the first tiles on their way
+    // before the set-up barrier (tensor memory is allocated meanwhile): Q_0 and
+    // K_0 first, which the first score GEMM needs, then Q_1 and V_0.  Paged K/V
+    // wait until after it: their page ids come from global memory, and the
+    // other warps would wait for those reads at the barrier.
+    constexpr bool kEarlyKV = !PAGED;
+    if (warp == kTmaWarp && lane == 0) {
         ctl.abort = 0;
         mbar_init(smem_u32(&ctl.q_full), 1);
+        mbar_init(smem_u32(&ctl.q0_full), 1);
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(smem_u32(&ctl.k_full[s]), 1);
             mbar_init(smem_u32(&ctl.k_empty[s]), 1);
@@ -461,6 +502,35 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         }
         mbar_init(smem_u32(&ctl.mma_done), 1);
         fence_mbar_init();
+        fence_proxy_async_smem();   // the initialised barriers, before the copies complete on them
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&tmO);
+        const uint32_t qbar = smem_u32(&ctl.q_full);
+        const bool q_weight = rope && a.q_w;
+        if (rope) {
+            // both tiles on one barrier: the softmax warps rotate them in place
+            mbar_arrive_expect_tx(qbar, 2 * kTileBytes + (q_weight ? D * 2 : 0));
+            if (q_weight)
+                bulk_load(sbase + kSmemW, a.q_w, D * 2, qbar);
+            load_q(0, qbar);
+        } else {
+            mbar_arrive_expect_tx(smem_u32(&ctl.q0_full), kTileBytes);
+            load_q(0, smem_u32(&ctl.q0_full));
+            mbar_arrive_expect_tx(qbar, kTileBytes);
+        }
+        if (kEarlyKV && w.n_kv > 0 && a.stall_tile != 0) {
+            const uint32_t kbar = smem_u32(&ctl.k_full[0]);
+            mbar_arrive_expect_tx(kbar, kTileBytes);
+            load_tile(&tmK, sbase + kSmemK, kbar, 0);
+        }
+        load_q(1, qbar);
+        if (kEarlyKV && w.n_kv > 0) {
+            const uint32_t vbar = smem_u32(&ctl.v_full[0]);
+            mbar_arrive_expect_tx(vbar, kTileBytes);
+            load_tile(&tmV, sbase + kSmemV, vbar, 0);
+        }
     }
     if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(&ctl.tmem_base), 512);
@@ -477,48 +547,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         if (warp == kTmaWarp) {
             // ------------------------------------------------------------ TMA producer
             if (lane == 0) {
-                tma_prefetch_desc(&tmQ);
-                tma_prefetch_desc(&tmK);
-                tma_prefetch_desc(&tmV);
-                tma_prefetch_desc(&tmO);
                 const uint32_t qbar = smem_u32(&ctl.q_full);
-                const bool q_weight = PAGED && a.rope && a.q_w;
-                mbar_arrive_expect_tx(qbar, 2 * kTileBytes + (q_weight ? D * 2 : 0));
-                if (q_weight)
-                    bulk_load(sbase + kSmemW, a.q_w, D * 2, qbar);
-                for (int t = 0; t < 2; ++t)
-                    for (int h = 0; h < 2; ++h) {
-                        const uint32_t dst = sbase + kSmemQ + t * kTileBytes + h * kBoxBytes;
-                        if (PAGED)
-                            tma_load_3d(dst, &tmQ, qbar, h * 64, w.head[t], w.q_base + w.row0[t]);
-                        else
-                            tma_load_4d(dst, &tmQ, qbar, h * 64, w.head[t], w.row0[t], w.b);
-                    }
-                const int* trow = PAGED ? a.block_tables + (size_t)w.b * a.max_blocks : nullptr;
-                // one K or V tile into `dst`: a 64 x 128 box per half (contiguous), or
-                // one 64 x 16 box per half and page (paged; a page past the context, or
-                // any id outside the cache, reads as zeros)
-                auto load_tile = [&](const CUtensorMap* map, uint32_t dst, uint32_t bar, int j) {
-                    if (PAGED) {
-                        int phys[kPagesPerTile];
-    #pragma unroll
-                        for (int k = 0; k < kPagesPerTile; ++k) {
-                            const int p = j * kPagesPerTile + k;
-                            phys[k] = p < w.n_pages ? trow[p] : -1;
-                        }
-    #pragma unroll
-                        for (int k = 0; k < kPagesPerTile; ++k)
-                            for (int h = 0; h < 2; ++h)
-                                tma_load_4d(dst + h * kBoxBytes + k * kPageBoxBytes, map, bar, h * 64, 0,
-                                            w.g, phys[k]);
-                    } else {
-                        for (int h = 0; h < 2; ++h)
-                            tma_load_4d(dst + h * kBoxBytes, map, bar, h * 64, w.g, j * BN, w.b);
-                    }
-                };
-                int n_k = 0, n_v = 0;  // K / V tiles issued so far
+                // contiguous: tile 0's K and V went out with the Q tiles
+                int n_k = kEarlyKV && w.n_kv > 0 ? 1 : 0, n_v = n_k;  // K / V tiles issued so far
                 bool ok = true;
-                for (int j = 0; j < w.n_kv && ok; ++j) {
+                for (int j = n_k; j < w.n_kv && ok; ++j) {
                     const int sk = j % kKStages;
                     ok = mbar_wait(smem_u32(&ctl.k_empty[sk]), ((j / kKStages) & 1) ^ 1, abort);
                     if (!ok)
@@ -544,6 +577,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 // is released (bounded by time only, not by the abort flag)
                 const int no_abort = 0;
                 mbar_wait(qbar, 0, &no_abort);
+                if (!rope)
+                    mbar_wait(smem_u32(&ctl.q0_full), 0, &no_abort);
                 for (int s = 0; s < kKStages; ++s) {
                     // loads issued into stage s: tiles j < n_k with j % kKStages == s,
                     // except a withheld one
@@ -619,8 +654,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             };
             // with the query prologue folded in, each tile's score GEMM waits for its
             // rows to be normalised and rotated (else for its TMA load)
-            const bool rope = PAGED && a.rope;
-            bool ok = wait(rope ? ctl.q_ready[0] : ctl.q_full, 0) && wait(ctl.k_full[0], 0);
+            bool ok = wait(rope ? ctl.q_ready[0] : ctl.q0_full, 0) && wait(ctl.k_full[0], 0);
             if (ok) {
                 tc_fence_after();
                 if (leader) {
@@ -629,7 +663,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 }
                 __syncwarp();
             }
-            ok = ok && (!rope || wait(ctl.q_ready[1], 0));
+            ok = ok && wait(rope ? ctl.q_ready[1] : ctl.q_full, 0);
             if (ok) {
                 tc_fence_after();
                 if (leader) {
