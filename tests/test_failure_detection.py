@@ -15,13 +15,16 @@ from gpu_util import assert_close, dev, host
 pytestmark = pytest.mark.gpu
 
 
-def test_withheld_tile_times_out_and_context_survives():
-    B, S, H_q, H_kv = 1, 256, 2, 1          # two CTAs; the one with two key tiles stalls on tile 1
+@pytest.mark.parametrize("stall_tile", [0, 1])
+def test_withheld_tile_times_out_and_context_survives(stall_tile):
+    # two CTAs; tile 0 (sent before the set-up barrier) stalls both, tile 1 the
+    # one with two key tiles
+    B, S, H_q, H_kv = 1, 256, 2, 1
     Q, K, V = W.prefill_inputs(W.PrefillConfig("t", B, S, H_q, H_kv), seed=3)
     dQ, dK, dV = dev(Q), dev(K), dev(V)
     O = torch.zeros(Q.shape, dtype=torch.float16, device="cuda")
     assert ag.attn_get_device_error(reset=True) == 0
-    ag.attn_debug_prefill_stall(dQ, dK, dV, O, stall_tile=1)
+    ag.attn_debug_prefill_stall(dQ, dK, dV, O, stall_tile=stall_tile)
     torch.cuda.synchronize()                 # returns: the waits are bounded
     code = ag.attn_get_device_error(reset=True)
     assert code & 1, f"expected the timeout bit, got {code}"
