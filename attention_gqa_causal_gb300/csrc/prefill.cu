@@ -224,7 +224,6 @@ struct SmemCtl {
     uint64_t v_full[kVStages], v_empty[kVStages];
     uint64_t s_full[2], p_full[2], o_full[2];
     uint64_t mma_done;
-    uint64_t epi_ready[2];   // a tile's O rows are in shared memory (128 arrivals)
     uint32_t tmem_base;
     int abort;
 };
@@ -498,7 +497,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             // tile 0's P barrier also takes the relay warp's arrival (operands in place)
             mbar_init(smem_u32(&ctl.p_full[t]), t == 0 ? 129 : 128);
             mbar_init(smem_u32(&ctl.o_full[t]), 1);
-            mbar_init(smem_u32(&ctl.epi_ready[t]), 128);
         }
         mbar_init(smem_u32(&ctl.mma_done), 1);
         fence_mbar_init();
@@ -938,12 +936,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         } else {
             tc_fence_after();
             const float inv = 1.f / l_sum;
-            // A whole tile leaves through shared memory and two TMA stores: Q_t's
+            // A whole tile leaves through shared memory and TMA stores: Q_t's
             // buffer is free (every S GEMM that read it completed before o_full),
             // each thread writes its row there in the 128-byte swizzled layout of
             // the O tensor map's boxes (conflict-free: 8 consecutive rows cover all
-            // 16-byte bank groups), and one thread stores the tile.  A tile that
-            // runs past the end of the sequence (chunk) stores its rows one by one.
+            // 16-byte bank groups), and each warp stores its 32 rows (two 64-dim
+            // boxes of 32 rows).  A tile that runs past the end of the sequence
+            // (chunk) stores its rows one by one.
             const bool whole = my_row0 + BM <= w.Lq;   // uniform over the warpgroup
             const bool store = q_row < w.Lq;
             __half* dst = a.O + ((size_t)(w.q_base + q_row) * a.H_q + my_head) * D;
@@ -971,22 +970,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 }
             }
             if (whole) {
-                // the storing thread waits (bounded) for all 128 rows; a warp that
-                // left on an abort never arrives, and then nothing is stored
+                // each warp stores its own 32 rows (1024-byte aligned inside the
+                // tile, so the swizzle phase is the tile's) once they are written
                 fence_proxy_async_smem();
-                mbar_arrive(smem_u32(&ctl.epi_ready[t]));
-                if (quad == 0 && lane == 0 && mbar_wait(smem_u32(&ctl.epi_ready[t]), 0, abort)) {
-                    const uint32_t src = sbase + kSmemQ + t * kTileBytes;
+                __syncwarp();
+                if (lane == 0) {
+                    const uint32_t src = sbase + kSmemQ + t * kTileBytes + quad * 32 * 128;
+                    const int r0 = my_row0 + quad * 32;
                     for (int h = 0; h < 2; ++h) {
                         if (PAGED)
-                            tma_store_3d(&tmO, src + h * kBoxBytes, h * 64, my_head, w.q_base + my_row0);
+                            tma_store_3d(&tmO, src + h * kBoxBytes, h * 64, my_head, w.q_base + r0);
                         else
-                            tma_store_4d(&tmO, src + h * kBoxBytes, h * 64, my_head, my_row0, w.b);
+                            tma_store_4d(&tmO, src + h * kBoxBytes, h * 64, my_head, r0, w.b);
                     }
                     bulk_commit_group();
                     bulk_wait_group_read0();   // shared memory stays valid until read
-                } else if (quad == 0 && lane == 0) {
-                    flag_abort(&ctl, a.err);
                 }
             }
         }
@@ -1037,22 +1035,23 @@ bool make_map(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
            CUDA_SUCCESS;
 }
 
-// [B,S,H,128]: boxes of 64 head-dim x 1 head x 128 rows x 1 batch.
-bool make_bshd_map(CUtensorMap* m, const void* ptr, int B, int S, int H)
+// [B,S,H,128]: boxes of 64 head-dim x 1 head x `rows` rows (128 for loads, 32
+// for the per-warp O stores) x 1 batch.
+bool make_bshd_map(CUtensorMap* m, const void* ptr, int B, int S, int H, int rows = BM)
 {
     const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
     const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2,
                                    (cuuint64_t)S * H * D * 2};
-    const cuuint32_t box[4] = {64, 1, BM, 1};
+    const cuuint32_t box[4] = {64, 1, (cuuint32_t)rows, 1};
     return make_map(m, ptr, 4, dims, strides, box);
 }
 
-// packed [total, H, 128]: boxes of 64 head-dim x 1 head x 128 rows.
-bool make_packed_map(CUtensorMap* m, const void* ptr, int total, int H)
+// packed [total, H, 128]: boxes of 64 head-dim x 1 head x `rows` rows.
+bool make_packed_map(CUtensorMap* m, const void* ptr, int total, int H, int rows = BM)
 {
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)total};
     const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
-    const cuuint32_t box[3] = {64, 1, BM};
+    const cuuint32_t box[3] = {64, 1, (cuuint32_t)rows};
     return make_map(m, ptr, 3, dims, strides, box);
 }
 
@@ -1134,7 +1133,7 @@ cudaError_t launch_prefill(const void* Q, const void* K, const void* V, void* O,
         return e;
     CUtensorMap mq, mk, mv, mo;
     if (!make_bshd_map(&mq, Q, B, S, H_q) || !make_bshd_map(&mk, K, B, S, H_kv) ||
-        !make_bshd_map(&mv, V, B, S, H_kv) || !make_bshd_map(&mo, O, B, S, H_q))
+        !make_bshd_map(&mv, V, B, S, H_kv) || !make_bshd_map(&mo, O, B, S, H_q, 32))
         return cudaErrorInvalidValue;
     PrefillArgs a{};
     a.O = static_cast<__half*>(O);
@@ -1163,7 +1162,7 @@ cudaError_t launch_prefill_paged(const void* Q, const void* k_cache, const void*
         return e;
     CUtensorMap mq, mk, mv, mo;
     if (!make_packed_map(&mq, Q, total_q, H_q) || !make_cache_map(&mk, k_cache, num_blocks, H_kv) ||
-        !make_cache_map(&mv, v_cache, num_blocks, H_kv) || !make_packed_map(&mo, O, total_q, H_q))
+        !make_cache_map(&mv, v_cache, num_blocks, H_kv) || !make_packed_map(&mo, O, total_q, H_q, 32))
         return cudaErrorInvalidValue;
     PrefillArgs a{};
     a.O = static_cast<__half*>(O);
