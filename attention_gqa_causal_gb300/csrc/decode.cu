@@ -12,8 +12,11 @@
 // identity worked through in the Kimi-K2.6 KernelBench trace.
 //
 // GB300 design.  The work is a stream of 4 KB page chunks per (page, kv head),
-// read once: it is HBM-bound (~2 FLOP/byte), so the kernel is built for
-// coalesced 16-byte loads and many bytes in flight, not for tensor cores.
+// read once.  With one or two query heads per kv head it is HBM-bound (~2
+// FLOP/byte), so decode_splitk_kernel is built for coalesced 16-byte loads and
+// many bytes in flight on CUDA cores.  The arithmetic grows with the group (2
+// FLOP per byte per query head): from three heads up, decode_mma_kernel (below)
+// packs the group into the rows of a warp-level tensor-core tile instead.
 //  * One CTA (4 warps) per (sequence, kv head, head chunk, split of
 //    `pages_per_split` pages).  Warps take pages round-robin.
 //  * All query heads of a GQA group that share the kv head are processed
@@ -317,6 +320,274 @@ decode_splitk_kernel(const __half* __restrict__ q, const __half* __restrict__ k_
     }
 }
 
+
+// ---------------------------------------------------------------------------
+// Groups of three or more query heads per kv head: the heads of a group form
+// the 16 rows (zero-padded) of a warp-level tensor-core tile.  Per 16-key page
+// a warp computes S[16 x 16] = Q K^T with 16 m16n8k16 MMAs and O[16 x 128] +=
+// P V with 16 more, so the arithmetic, which outgrows the CUDA cores at ~8
+// FLOP per K/V byte for 8 heads, costs a few hundred cycles per 8 KB page.
+// Pages reach shared memory by 16-byte asynchronous copies into a two-stage
+// ring per warp, rows swizzled (16-byte chunk c of key r at c ^ (r % 8)) so the
+// matrix loads are conflict-free.  Same units, partials and combine as above.
+constexpr int kMmaHeads = 16;                       // tile rows: heads per CTA
+constexpr int kMmaStages = 2;                       // pages in flight per warp
+constexpr int kPageBytes = kPageSize * kHeadDim * 2;    // one (page, kv head) of K or V: 4 KB
+constexpr int kMmaStageBytes = 2 * kPageBytes;          // K and V
+constexpr int kMmaSmemBytes = kDecodeWarps * kMmaStages * kMmaStageBytes;   // 64 KB
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr) : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr) : "memory");
+}
+// D (16x8, FP32) += A (16x16, FP16, row) * B (16x8, FP16, col)
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi)
+{
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+// byte offset of 16-byte chunk c of key row r in a swizzled 16 x 256-byte page
+__device__ __forceinline__ uint32_t swz(int r, int c) { return (uint32_t)(r * 256 + ((c ^ (r & 7)) << 4)); }
+
+__global__ void __launch_bounds__(kDecodeWarps * 32, 3)
+decode_mma_kernel(const __half* __restrict__ q, const __half* __restrict__ k_cache,
+                  const __half* __restrict__ v_cache, const int* __restrict__ block_tables,
+                  const int* __restrict__ seq_lens, float* __restrict__ O_part,
+                  float* __restrict__ lse_part, int H_q, int H_kv, int group, int chunks,
+                  int max_blocks_per_seq, int pages_per_split, int n_split, float scale_log2)
+{
+    constexpr int D = kHeadDim;
+    constexpr int BS = kPageSize;
+    extern __shared__ __align__(128) unsigned char dsm[];
+    grid_dependency_wait();   // the cache may have been written by the launch before (KV append)
+    allow_dependents();       // the combine may be scheduled once every CTA has started
+    const int split = blockIdx.x % n_split;
+    int rest = blockIdx.x / n_split;
+    const int chunk = rest % chunks;
+    rest /= chunks;
+    const int g = rest % H_kv;
+    const int n = rest / H_kv;
+
+    int L = seq_lens[n];
+    const int max_len = max_blocks_per_seq * BS;
+    if (L > max_len) {
+        if (threadIdx.x == 0 && split == 0 && g == 0 && chunk == 0)
+            atomicOr(&g_device_error, kDevErrSeqTooLong);
+        L = max_len;
+    }
+    const int n_pages = (L + BS - 1) / BS;
+    const int p_begin = split * pages_per_split;
+    if (p_begin >= n_pages)
+        return;  // empty split: the combine kernel does not read it
+    const int p_end = min(n_pages, p_begin + pages_per_split);
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const int gid = lane >> 2;   // fragment row group
+    const int tig = lane & 3;    // thread in group
+    const int h0 = g * group + chunk * kMmaHeads;
+    const int n_heads = min(kMmaHeads, group - chunk * kMmaHeads);
+
+    // Q as A fragments, rows gid and gid + 8 (zero past the group), 8 K-steps of 16 dims
+    uint32_t qa[8][4];
+    {
+        const uint32_t* q0 = reinterpret_cast<const uint32_t*>(q + ((size_t)n * H_q + h0 + gid) * D);
+        const uint32_t* q1 = reinterpret_cast<const uint32_t*>(q + ((size_t)n * H_q + h0 + gid + 8) * D);
+        const bool v0 = gid < n_heads, v1 = gid + 8 < n_heads;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            qa[kk][0] = v0 ? q0[kk * 8 + tig] : 0u;
+            qa[kk][1] = v1 ? q1[kk * 8 + tig] : 0u;
+            qa[kk][2] = v0 ? q0[kk * 8 + 4 + tig] : 0u;
+            qa[kk][3] = v1 ? q1[kk * 8 + 4 + tig] : 0u;
+        }
+    }
+
+    const uint32_t ring = smem_u32(dsm) + warp * kMmaStages * kMmaStageBytes;
+    const int* table = block_tables + (size_t)n * max_blocks_per_seq;
+    const size_t page_stride = (size_t)H_kv * BS * D;  // halves per physical block
+
+    // issue the copies of this warp's i-th page (an empty group for a bad or
+    // missing one); V rows past the context are zeroed instead (their slots may
+    // hold anything, and 0 * NaN would reach O through the MMA)
+    auto issue = [&](int i) {
+        const int p = p_begin + warp + i * kDecodeWarps;
+        if (p < p_end) {
+            const int phys = table[p];
+            if (phys >= 0) {
+                const int valid = min(BS, L - p * BS);
+                const size_t base = (size_t)phys * page_stride + (size_t)g * BS * D;
+                const uint32_t kst = ring + (i % kMmaStages) * kMmaStageBytes;
+                const uint32_t vst = kst + kPageBytes;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int ci = lane + 32 * u;        // 16-byte chunk of the 4 KB page
+                    const int r = ci >> 4, c = ci & 15;
+                    cp_async16(kst + swz(r, c), k_cache + base + r * D + c * 8);
+                    if (r < valid)
+                        cp_async16(vst + swz(r, c), v_cache + base + r * D + c * 8);
+                    else
+                        asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(vst + swz(r, c)), "r"(0u) : "memory");
+                }
+            }
+        }
+        cp_async_commit();
+    };
+
+    float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F;   // rows gid, gid + 8 (log2 units)
+    float l0 = 0.f, l1 = 0.f;                       // this thread's share of the row sums
+    float o[16][4];
+#pragma unroll
+    for (int nb = 0; nb < 16; ++nb)
+        o[nb][0] = o[nb][1] = o[nb][2] = o[nb][3] = 0.f;
+
+    const int my_pages = p_begin + warp < p_end ? (p_end - p_begin - warp + kDecodeWarps - 1) / kDecodeWarps : 0;
+#pragma unroll
+    for (int i = 0; i < kMmaStages - 1; ++i)
+        issue(i);
+    for (int i = 0; i < my_pages; ++i) {
+        issue(i + kMmaStages - 1);
+        cp_async_wait<kMmaStages - 1>();
+        __syncwarp();
+        const int p = p_begin + warp + i * kDecodeWarps;
+        const int phys = table[p];
+        if (phys < 0) {
+            if (lane == 0)
+                atomicOr(&g_device_error, kDevErrBadBlockId);
+            __syncwarp();
+            continue;
+        }
+        const int valid = min(BS, L - p * BS);
+        const uint32_t kst = ring + (i % kMmaStages) * kMmaStageBytes;
+        const uint32_t vst = kst + kPageBytes;
+        const int r8 = lane & 7, mi = lane >> 3;
+        // S = Q K^T: n-blocks of keys 0-7 and 8-15
+        float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            uint32_t b0, b1, b2, b3;
+            const int key = ((mi >> 1) << 3) + r8;
+            ldsm_x4(kst + swz(key, (kk << 1) + (mi & 1)), b0, b1, b2, b3);
+            mma16816(s[0], qa[kk], b0, b1);
+            mma16816(s[1], qa[kk], b2, b3);
+        }
+        // online softmax over the page's keys (log2 units), rows gid and gid + 8
+        float x[2][4];
+#pragma unroll
+        for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int key = nb * 8 + tig * 2 + (e & 1);
+                x[nb][e] = key < valid ? s[nb][e] * scale_log2 : -CUDART_INF_F;
+            }
+        float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
+        float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);   // finite: key 0 of a page is valid
+        const float a0 = ex2_approx(m0 - mn0), a1 = ex2_approx(m1 - mn1);
+        m0 = mn0;
+        m1 = mn1;
+        float pr[2][4];
+#pragma unroll
+        for (int nb = 0; nb < 2; ++nb) {
+            pr[nb][0] = ex2_approx(x[nb][0] - mn0);
+            pr[nb][1] = ex2_approx(x[nb][1] - mn0);
+            pr[nb][2] = ex2_approx(x[nb][2] - mn1);
+            pr[nb][3] = ex2_approx(x[nb][3] - mn1);
+        }
+        l0 = l0 * a0 + (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
+        l1 = l1 * a1 + (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
+        const uint32_t pa[4] = {pack_h2(pr[0][0], pr[0][1]), pack_h2(pr[0][2], pr[0][3]),
+                                pack_h2(pr[1][0], pr[1][1]), pack_h2(pr[1][2], pr[1][3])};
+        // O = O * alpha + P V, in n-blocks of 8 dims
+#pragma unroll
+        for (int nb = 0; nb < 16; nb += 2) {
+            uint32_t b0, b1, b2, b3;
+            const int key = ((mi & 1) << 3) + r8;
+            ldsm_x4_t(vst + swz(key, nb + (mi >> 1)), b0, b1, b2, b3);
+            o[nb][0] *= a0; o[nb][1] *= a0; o[nb][2] *= a1; o[nb][3] *= a1;
+            o[nb + 1][0] *= a0; o[nb + 1][1] *= a0; o[nb + 1][2] *= a1; o[nb + 1][3] *= a1;
+            mma16816(o[nb], pa, b0, b1);
+            mma16816(o[nb + 1], pa, b2, b3);
+        }
+        __syncwarp();   // every lane has read this stage before it is refilled
+    }
+    cp_async_wait<0>();
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    __syncthreads();   // the rings are free: reuse them for the merge
+
+    // merge the 4 warps through shared memory
+    float* sm_o = reinterpret_cast<float*>(dsm);                          // [warp][16][D]
+    float* sm_m = sm_o + kDecodeWarps * kMmaHeads * D;                     // [warp][16]
+    float* sm_l = sm_m + kDecodeWarps * kMmaHeads;                         // [warp][16]
+#pragma unroll
+    for (int nb = 0; nb < 16; ++nb) {
+        const int d = nb * 8 + tig * 2;
+        sm_o[(warp * kMmaHeads + gid) * D + d] = o[nb][0];
+        sm_o[(warp * kMmaHeads + gid) * D + d + 1] = o[nb][1];
+        sm_o[(warp * kMmaHeads + gid + 8) * D + d] = o[nb][2];
+        sm_o[(warp * kMmaHeads + gid + 8) * D + d + 1] = o[nb][3];
+    }
+    if (tig == 0) {
+        sm_m[warp * kMmaHeads + gid] = m0;
+        sm_m[warp * kMmaHeads + gid + 8] = m1;
+        sm_l[warp * kMmaHeads + gid] = l0;
+        sm_l[warp * kMmaHeads + gid + 8] = l1;
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < n_heads * D; idx += blockDim.x) {
+        const int hh = idx / D, d = idx % D;
+        float M = -CUDART_INF_F;
+#pragma unroll
+        for (int w = 0; w < kDecodeWarps; ++w)
+            M = fmaxf(M, sm_m[w * kMmaHeads + hh]);
+        const size_t row = (size_t)n * H_q + h0 + hh;
+        if (M == -CUDART_INF_F) {
+            // every page of this split had a negative block id: an empty segment
+            O_part[(row * n_split + split) * D + d] = 0.f;
+            if (d == 0)
+                lse_part[row * n_split + split] = -CUDART_INF_F;
+            continue;
+        }
+        float Lsum = 0.f, acc = 0.f;
+#pragma unroll
+        for (int w = 0; w < kDecodeWarps; ++w) {
+            const float c = ex2_approx(sm_m[w * kMmaHeads + hh] - M);  // 0 for a warp with no pages
+            Lsum += c * sm_l[w * kMmaHeads + hh];
+            acc += c * sm_o[(w * kMmaHeads + hh) * D + d];
+        }
+        O_part[(row * n_split + split) * D + d] = acc / Lsum;
+        if (d == 0)
+            lse_part[row * n_split + split] = (M + __log2f(Lsum)) * kLn2;
+    }
+}
+
 // One CTA of kCombineWarps warps per output row; lane owns 4 consecutive
 // head-dim entries.  The warps take the row's splits round-robin (loads
 // unrolled for memory-level parallelism) and are merged in shared memory.
@@ -413,13 +684,14 @@ lse_combine_kernel(const float* __restrict__ O_part, const float* __restrict__ l
     }
 }
 
+// Larger groups run as several 4-head chunks over the same pages: an 8-head
+// CTA needs more registers than a thread has (it spilled and ran 2 CTAs per SM),
+// and its chunks read the same K/V close together in time, from L2.
 int pick_heads_per_cta(int group)
 {
     if (group <= 2)
         return group;
-    if (group <= 4)
-        return 4;
-    return 8;
+    return kMmaHeads;
 }
 
 // SMs of the current device; a GB300's 152 if it cannot be queried (the
@@ -505,6 +777,35 @@ static cudaError_t launch_main(const DecodePlan& p, const void* q, const void* k
                               p.max_blocks_per_seq, p.pages_per_split, p.n_split, q_scale);
 }
 
+static cudaError_t launch_main_mma(const DecodePlan& p, const void* q, const void* k_cache,
+                                   const void* v_cache, const int* block_tables, const int* seq_lens,
+                                   float* O_part, float* lse_part, cudaStream_t stream)
+{
+    const long long grid = (long long)p.num_seqs * p.H_kv * p.chunks * p.n_split;
+    if (grid > 0x7fffffffLL)
+        return cudaErrorInvalidConfiguration;
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 64 && !attr_done[dev]) {
+        e = cudaFuncSetAttribute(decode_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmemBytes);
+        if (e != cudaSuccess)
+            return e;
+        attr_done[dev] = true;
+    }
+    const float scale_log2 = kLog2e / sqrtf((float)kHeadDim);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    dependent_launch(cfg, attr, dim3((unsigned)grid), dim3(kDecodeWarps * 32), stream);
+    cfg.dynamicSmemBytes = kMmaSmemBytes;
+    return cudaLaunchKernelEx(&cfg, decode_mma_kernel, static_cast<const __half*>(q),
+                              static_cast<const __half*>(k_cache), static_cast<const __half*>(v_cache),
+                              block_tables, seq_lens, O_part, lse_part, p.H_q, p.H_kv, p.group, p.chunks,
+                              p.max_blocks_per_seq, p.pages_per_split, p.n_split, scale_log2);
+}
+
 cudaError_t launch_decode(const DecodePlan& p, const void* q, const void* k_cache,
                           const void* v_cache, void* out, const int* block_tables,
                           const int* seq_lens, void* ws, cudaStream_t stream)
@@ -516,8 +817,7 @@ cudaError_t launch_decode(const DecodePlan& p, const void* q, const void* k_cach
     switch (p.heads_per_cta) {
     case 1: e = launch_main<1>(p, q, k_cache, v_cache, block_tables, seq_lens, O_part, lse_part, stream); break;
     case 2: e = launch_main<2>(p, q, k_cache, v_cache, block_tables, seq_lens, O_part, lse_part, stream); break;
-    case 4: e = launch_main<4>(p, q, k_cache, v_cache, block_tables, seq_lens, O_part, lse_part, stream); break;
-    default: e = launch_main<8>(p, q, k_cache, v_cache, block_tables, seq_lens, O_part, lse_part, stream); break;
+    default: e = launch_main_mma(p, q, k_cache, v_cache, block_tables, seq_lens, O_part, lse_part, stream); break;
     }
     if (e != cudaSuccess)
         return e;

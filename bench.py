@@ -14,8 +14,10 @@ One step is one pass over every hot-path kernel on its workload:
   * the chunked prefill alone (FLOPs over each query's visible keys); it runs
     just before the decode legs, as it leaves the least dirty data in L2
   * paged decode          256 sequences, lengths uniform on [128, 2048], H 16/8
-  * paged decode          8 sequences x 32768 tokens, H 16/8
   * the 256-sequence decode step together with its KV append (two launches)
+  * paged decode          8 sequences x 32768 tokens, H 16/8
+  * paged decode          256 sequences as above, H 64/8 (eight query heads per
+    kv head: the tensor-core decode kernel)
     (decode: GB/s of K/V bytes of the valid tokens; split-K + combine kernels)
   * the attention-input prologue (QK-norm, RoPE, KV append) of 2 x 8192 new
     tokens, H 32/8 (GB/s of the bytes it must move)
@@ -55,6 +57,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 KERNEL_SOURCES = {
     "prefill_kernel": ["prefill.cu", "ptx.cuh"],
     "decode_splitk_kernel": ["decode.cu"],
+    "decode_mma_kernel": ["decode.cu"],
     "qk_norm_rope_kernel": ["rope.cu", "ptx.cuh"],
 }
 
@@ -308,7 +311,7 @@ def build_legs(torch, ag, which):
                       "H_q": cfg.H_q, "H_kv": cfg.H_kv, "D": cfg.D, "causal": cfg.causal,
                       "block_size": 16, "num_blocks": int(kc.shape[0])}
         legs.append(leg)
-    for cfg, key in ((W.DECODE_MIX, "decode"), (W.DECODE_LONG, "decode_long")):
+    for cfg, key in ((W.DECODE_MIX, "decode"), (W.DECODE_LONG, "decode_long"), (W.DECODE_GQA8, "decode_gqa8")):
         if which not in ("all", key) and not (key == "decode" and which == "decode_append"):
             continue
         inp = W.decode_inputs(cfg, seed=0)
@@ -316,6 +319,8 @@ def build_legs(torch, ag, which):
                                                   inp.block_tables, inp.seq_lens)]
         out = torch.empty_like(t[0])
         leg = Leg(cfg.name, "decode", float(inp.kv_bytes()), "GB/s", 2)
+        # groups of three or more heads per kv head take the tensor-core kernel
+        leg.kernel = "decode_mma_kernel" if cfg.H_q // cfg.H_kv >= 3 else "decode_splitk_kernel"
         leg.set_buffers(lambda t, o: (lambda: ag.attn_decode_paged(t[0], t[1], t[2], o, t[3], t[4])),
                         tuple(t), out)
         leg.host = {"q": inp.q, "k_cache": inp.k_cache, "v_cache": inp.v_cache,
@@ -583,7 +588,7 @@ def run_ours(args):
                                 "traffic": dram_traffic("prefill_kernel", leg.name)}
         else:
             peak = peaks["hbm_gbs"]
-            kernel = "qk_norm_rope_kernel" if leg.kind == "prologue" else "decode_splitk_kernel"
+            kernel = "qk_norm_rope_kernel" if leg.kind == "prologue" else getattr(leg, "kernel", "decode_splitk_kernel")
             part["roofline"] = {"bound": "hbm", "achieved": leg.value(ms), "peak": peak,
                                 "unit": "GB/s", "frac": leg.value(ms) / peak,
                                 "peak_kind": f"{peak_src} copy bandwidth",
@@ -668,7 +673,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["all", "prefill", "prefill_full", "prefill_paged", "layer", "prologue", "qwen",
-                                           "decode", "decode_long", "decode_append"],
+                                           "decode", "decode_long", "decode_append", "decode_gqa8"],
                     default="all")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="CPU time budget of the oracle baseline sample")

@@ -143,6 +143,8 @@ PREFILL_LONG_FULL = PrefillConfig("prefill_b2_s8192_h32_kv8_full", 2, 8192, 32, 
 DECODE_MIX = DecodeConfig("decode_n256_len128to2048_h16_kv8", 256, 16, 8)
 DECODE_LONG = DecodeConfig("decode_n8_len32768_h16_kv8", 8, 16, 8, len_lo=32768,
                            len_hi=32768, max_blocks_per_seq=2048)
+# the same length mix with eight query heads per kv head (a GQA-8 model's decode)
+DECODE_GQA8 = DecodeConfig("decode_n256_len128to2048_h64_kv8", 256, 64, 8)
 
 
 def prefill_inputs(cfg: PrefillConfig, seed: int = 0):
