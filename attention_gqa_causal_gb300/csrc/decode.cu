@@ -543,16 +543,17 @@ decode_mma_kernel(const __half* __restrict__ q, const __half* __restrict__ k_cac
     __syncthreads();   // the rings are free: reuse them for the merge
 
     // merge the 4 warps through shared memory
-    float* sm_o = reinterpret_cast<float*>(dsm);                          // [warp][16][D]
-    float* sm_m = sm_o + kDecodeWarps * kMmaHeads * D;                     // [warp][16]
+    // rows padded to 136 floats: the 8-byte stores of a half-warp (4 rows x 4
+    // pairs) then fall on distinct banks
+    constexpr int SO = D + 8;
+    float* sm_o = reinterpret_cast<float*>(dsm);                          // [warp][16][SO]
+    float* sm_m = sm_o + kDecodeWarps * kMmaHeads * SO;                    // [warp][16]
     float* sm_l = sm_m + kDecodeWarps * kMmaHeads;                         // [warp][16]
 #pragma unroll
     for (int nb = 0; nb < 16; ++nb) {
         const int d = nb * 8 + tig * 2;
-        sm_o[(warp * kMmaHeads + gid) * D + d] = o[nb][0];
-        sm_o[(warp * kMmaHeads + gid) * D + d + 1] = o[nb][1];
-        sm_o[(warp * kMmaHeads + gid + 8) * D + d] = o[nb][2];
-        sm_o[(warp * kMmaHeads + gid + 8) * D + d + 1] = o[nb][3];
+        *reinterpret_cast<float2*>(&sm_o[(warp * kMmaHeads + gid) * SO + d]) = make_float2(o[nb][0], o[nb][1]);
+        *reinterpret_cast<float2*>(&sm_o[(warp * kMmaHeads + gid + 8) * SO + d]) = make_float2(o[nb][2], o[nb][3]);
     }
     if (tig == 0) {
         sm_m[warp * kMmaHeads + gid] = m0;
@@ -580,7 +581,7 @@ decode_mma_kernel(const __half* __restrict__ q, const __half* __restrict__ k_cac
         for (int w = 0; w < kDecodeWarps; ++w) {
             const float c = ex2_approx(sm_m[w * kMmaHeads + hh] - M);  // 0 for a warp with no pages
             Lsum += c * sm_l[w * kMmaHeads + hh];
-            acc += c * sm_o[(w * kMmaHeads + hh) * D + d];
+            acc += c * sm_o[(w * kMmaHeads + hh) * SO + d];
         }
         O_part[(row * n_split + split) * D + d] = acc / Lsum;
         if (d == 0)
@@ -684,9 +685,77 @@ lse_combine_kernel(const float* __restrict__ O_part, const float* __restrict__ l
     }
 }
 
-// Larger groups run as several 4-head chunks over the same pages: an 8-head
-// CTA needs more registers than a thread has (it spilled and ran 2 CTAs per SM),
-// and its chunks read the same K/V close together in time, from L2.
+// The same merge with one warp per row, four rows per CTA: for rows of a few
+// splits (the common case) the one-CTA-per-row form is dominated by launching
+// and synchronising CTAs.  Each lane owns 4 head-dim entries.
+__global__ void __launch_bounds__(kCombineWarps * 32)
+lse_combine_rows_kernel(const float* __restrict__ O_part, const float* __restrict__ lse_part,
+                        __half* __restrict__ out, int R, int n_split, const int* __restrict__ seq_lens,
+                        int H_q, int pages_per_split, int max_len)
+{
+    constexpr int D = kHeadDim;
+    grid_dependency_wait();   // the partials come from the launch before
+    const int row = blockIdx.x * kCombineWarps + threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    if (row >= R)
+        return;
+    int ns = n_split;
+    if (seq_lens) {
+        const int L = min(seq_lens[row / H_q], max_len);
+        const int pages = (L + kPageSize - 1) / kPageSize;
+        ns = (pages + pages_per_split - 1) / pages_per_split;
+    }
+    const float* lp = lse_part + (size_t)row * n_split;
+    const float* op = O_part + (size_t)row * n_split * D + lane * 4;
+    float M = -CUDART_INF_F;
+    for (int i = lane; i < ns; i += 32)
+        M = fmaxf(M, lp[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float wsum = 0.f;
+    if (M != -CUDART_INF_F) {
+        const float Ml = M * kLog2e;
+        int i = 0;
+        for (; i + 3 < ns; i += 4) {
+            float wt[4];
+            float4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                wt[u] = lp[i + u];
+                v[u] = *reinterpret_cast<const float4*>(op + (size_t)(i + u) * D);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float w = ex2_approx(fmaf(wt[u], kLog2e, -Ml));
+                wsum += w;
+                acc.x = fmaf(w, v[u].x, acc.x);
+                acc.y = fmaf(w, v[u].y, acc.y);
+                acc.z = fmaf(w, v[u].z, acc.z);
+                acc.w = fmaf(w, v[u].w, acc.w);
+            }
+        }
+        for (; i < ns; ++i) {
+            const float w = ex2_approx(fmaf(lp[i], kLog2e, -Ml));
+            const float4 v = *reinterpret_cast<const float4*>(op + (size_t)i * D);
+            wsum += w;
+            acc.x = fmaf(w, v.x, acc.x);
+            acc.y = fmaf(w, v.y, acc.y);
+            acc.z = fmaf(w, v.z, acc.z);
+            acc.w = fmaf(w, v.w, acc.w);
+        }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;  // all segments empty -> zeros
+    __half2 h[2] = {__floats2half2_rn(acc.x * inv, acc.y * inv), __floats2half2_rn(acc.z * inv, acc.w * inv)};
+    *reinterpret_cast<uint2*>(out + (size_t)row * D + lane * 4) = *reinterpret_cast<uint2*>(h);
+}
+
+// Rows of at most this many splits are merged one warp per row.
+constexpr int kRowsCombineMaxSplits = 8;
+
+// One or two query heads per kv head: the CUDA-core kernel, all heads of the
+// group in one CTA.  Three or more: the tensor-core kernel's 16-row head tiles.
 int pick_heads_per_cta(int group)
 {
     if (group <= 2)
@@ -824,6 +893,13 @@ cudaError_t launch_decode(const DecodePlan& p, const void* q, const void* k_cach
     const int R = p.num_seqs * p.H_q;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
+    if (p.n_split <= kRowsCombineMaxSplits) {
+        dependent_launch(cfg, attr, dim3((unsigned)((R + kCombineWarps - 1) / kCombineWarps)),
+                         dim3(kCombineWarps * 32), stream);
+        return cudaLaunchKernelEx(&cfg, lse_combine_rows_kernel, (const float*)O_part, (const float*)lse_part,
+                                  static_cast<__half*>(out), R, p.n_split, seq_lens, p.H_q, p.pages_per_split,
+                                  p.max_blocks_per_seq * kPageSize);
+    }
     dependent_launch(cfg, attr, dim3((unsigned)R), dim3(kCombineWarps * 32), stream);
     return cudaLaunchKernelEx(&cfg, lse_combine_kernel, (const float*)O_part, (const float*)lse_part,
                               static_cast<__half*>(out), p.n_split, seq_lens, p.H_q, p.pages_per_split,
@@ -833,8 +909,12 @@ cudaError_t launch_decode(const DecodePlan& p, const void* q, const void* k_cach
 cudaError_t launch_lse_combine(const float* O_part, const float* lse_part, void* out, int R,
                                int n_split, cudaStream_t stream)
 {
-    lse_combine_kernel<<<R, kCombineWarps * 32, 0, stream>>>(
-        O_part, lse_part, static_cast<__half*>(out), n_split, nullptr, 1, 1, 0);
+    if (n_split <= kRowsCombineMaxSplits)
+        lse_combine_rows_kernel<<<(R + kCombineWarps - 1) / kCombineWarps, kCombineWarps * 32, 0, stream>>>(
+            O_part, lse_part, static_cast<__half*>(out), R, n_split, nullptr, 1, 1, 0);
+    else
+        lse_combine_kernel<<<R, kCombineWarps * 32, 0, stream>>>(
+            O_part, lse_part, static_cast<__half*>(out), n_split, nullptr, 1, 1, 0);
     return cudaGetLastError();
 }
 
