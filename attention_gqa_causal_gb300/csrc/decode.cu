@@ -12,21 +12,21 @@
 // identity worked through in the Kimi-K2.6 KernelBench trace.
 //
 // GB300 design.  The work is a stream of 4 KB page chunks per (page, kv head),
-// read once.  With one or two query heads per kv head it is HBM-bound (~2
-// FLOP/byte), so decode_splitk_kernel is built for coalesced 16-byte loads and
-// many bytes in flight on CUDA cores.  The arithmetic grows with the group (2
-// FLOP per byte per query head): from three heads up, decode_mma_kernel (below)
-// packs the group into the rows of a warp-level tensor-core tile instead.
-//  * One CTA (4 warps) per (sequence, kv head, head chunk, split of
-//    `pages_per_split` pages).  Warps take pages round-robin.
-//  * All query heads of a GQA group that share the kv head are processed
-//    against each loaded page, so every K/V byte is read from HBM once.
-//  * Lane l of a warp owns tokens {l/16 + 2i} and head-dim slice
-//    [(l%16)*8, +8) of a page: each load instruction of the warp covers two
-//    full 256-byte token rows (coalesced), and every lane issues 8+8 16-byte
-//    loads per page.
-//  * Scores are in log2 units (q is pre-scaled by log2(e)/sqrt(D)); exp2 uses
-//    the MUFU ex2 instruction.
+// read once, so it is HBM-bound while the arithmetic per byte stays low: 2
+// FLOP per K/V byte for each query head that shares the kv head.
+//  * One CTA (4 warps) per (sequence, kv head, chunk of up to 16 query heads,
+//    split of `pages_per_split` pages).  Warps take pages round-robin.
+//  * The query heads of a GQA group form the rows (zero-padded to 16) of a
+//    warp-level tensor-core tile: per 16-key page a warp computes
+//    S[16 x 16] = Q K^T with 16 m16n8k16 MMAs and O[16 x 128] += P V with 16
+//    more, so every K/V byte is read from HBM once for all heads of its group
+//    and the arithmetic stays a small fraction of a page's load time at any
+//    group size (on CUDA cores it overtook the loads from four heads up).
+//  * Pages reach shared memory by 16-byte asynchronous copies into a
+//    two-stage ring per warp (3 CTAs and ~190 KB in flight per SM), rows
+//    swizzled so the matrix loads that feed the MMAs are conflict-free.
+//  * Scores are in log2 units (scale log2(e)/sqrt(D) applied to the FP32
+//    scores); P is rounded to FP16 for the PV MMA; exp2 uses MUFU ex2.
 //  * The CTA merges its 4 warps in shared memory and writes one partial
 //    (O normalised, lse natural log) per head; the combine kernel merges the
 //    splits.  Empty splits (past the end of a sequence) exit at once and are
@@ -36,6 +36,7 @@
 //    scheduled as soon as its own CTAs have started, and the dependent waits on
 //    the device for its results, so the launch gaps overlap the tails.
 #include <cstdint>
+#include <mutex>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
@@ -88,248 +89,9 @@ __device__ __forceinline__ void allow_dependents()
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-__device__ __forceinline__ uint4 ld_stream16(const void* p)
-{
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
-__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8])
-{
-    const __half2* h = reinterpret_cast<const __half2*>(&v);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 t = __half22float2(h[i]);
-        f[2 * i] = t.x;
-        f[2 * i + 1] = t.y;
-    }
-}
-
-// Sum over the 16 lanes of each half-warp.
-__device__ __forceinline__ float half_warp_sum(float x)
-{
-    x += __shfl_xor_sync(0xffffffffu, x, 8);
-    x += __shfl_xor_sync(0xffffffffu, x, 4);
-    x += __shfl_xor_sync(0xffffffffu, x, 2);
-    x += __shfl_xor_sync(0xffffffffu, x, 1);
-    return x;
-}
-
-// GP: query heads per CTA (>= 1).  Heads beyond the group are computed on
-// zero queries and not written.
-template <int GP>
-__global__ void __launch_bounds__(kDecodeWarps * 32)
-decode_splitk_kernel(const __half* __restrict__ q, const __half* __restrict__ k_cache,
-                     const __half* __restrict__ v_cache, const int* __restrict__ block_tables,
-                     const int* __restrict__ seq_lens, float* __restrict__ O_part,
-                     float* __restrict__ lse_part, int H_q, int H_kv, int group, int chunks,
-                     int max_blocks_per_seq, int pages_per_split, int n_split, float q_scale)
-{
-    constexpr int D = kHeadDim;
-    constexpr int BS = kPageSize;
-    grid_dependency_wait();   // the cache may have been written by the launch before (KV append)
-    allow_dependents();       // the combine may be scheduled once every CTA has started
-    const int split = blockIdx.x % n_split;
-    int rest = blockIdx.x / n_split;
-    const int chunk = rest % chunks;
-    rest /= chunks;
-    const int g = rest % H_kv;
-    const int n = rest / H_kv;
-
-    int L = seq_lens[n];
-    const int max_len = max_blocks_per_seq * BS;
-    if (L > max_len) {
-        if (threadIdx.x == 0 && split == 0 && g == 0 && chunk == 0)
-            atomicOr(&g_device_error, kDevErrSeqTooLong);
-        L = max_len;
-    }
-    const int n_pages = (L + BS - 1) / BS;
-    const int p_begin = split * pages_per_split;
-    if (p_begin >= n_pages)
-        return;  // empty split: the combine kernel does not read it
-    const int p_end = min(n_pages, p_begin + pages_per_split);
-
-    const int warp = threadIdx.x / 32;
-    const int lane = threadIdx.x % 32;
-    const int half = lane / 16;         // token parity within a page
-    const int dofs = (lane % 16) * 8;   // head-dim slice
-    const int h0 = g * group + chunk * GP;
-    const int n_heads = min(GP, group - chunk * GP);
-
-    // this lane's query slices, pre-scaled so scores come out in log2 units
-    float qf[GP][8];
-#pragma unroll
-    for (int hh = 0; hh < GP; ++hh) {
-        if (hh < n_heads) {
-            const uint4 v = *reinterpret_cast<const uint4*>(q + ((size_t)n * H_q + h0 + hh) * D + dofs);
-            unpack8(v, qf[hh]);
-#pragma unroll
-            for (int d = 0; d < 8; ++d)
-                qf[hh][d] *= q_scale;
-        } else {
-#pragma unroll
-            for (int d = 0; d < 8; ++d)
-                qf[hh][d] = 0.f;
-        }
-    }
-
-    float m[GP], l[GP], o[GP][8];
-#pragma unroll
-    for (int hh = 0; hh < GP; ++hh) {
-        m[hh] = -CUDART_INF_F;
-        l[hh] = 0.f;
-#pragma unroll
-        for (int d = 0; d < 8; ++d)
-            o[hh][d] = 0.f;
-    }
-
-    const int* table = block_tables + (size_t)n * max_blocks_per_seq;
-    const size_t page_stride = (size_t)H_kv * BS * D;  // halves per physical block
-    for (int p = p_begin + warp; p < p_end; p += kDecodeWarps) {
-        int phys = table[p];
-        const bool bad = phys < 0;
-        if (bad) {
-            if (lane == 0)
-                atomicOr(&g_device_error, kDevErrBadBlockId);
-            continue;
-        }
-        const size_t base = (size_t)phys * page_stride + (size_t)g * BS * D + dofs;
-        const __half* kp = k_cache + base;
-        const __half* vp = v_cache + base;
-        uint4 kr[8], vr[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            kr[i] = ld_stream16(kp + (size_t)(half + 2 * i) * D);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            vr[i] = ld_stream16(vp + (size_t)(half + 2 * i) * D);
-
-        const int valid = L - p * BS;  // tokens of this page inside the context (>= 1)
-        // scores s[i][hh] for token half + 2i (identical on the 16 lanes of a half-warp)
-        float s[8][GP];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            float kf[8];
-            unpack8(kr[i], kf);
-#pragma unroll
-            for (int hh = 0; hh < GP; ++hh) {
-                float acc = 0.f;
-#pragma unroll
-                for (int d = 0; d < 8; ++d)
-                    acc = fmaf(qf[hh][d], kf[d], acc);
-                s[i][hh] = half_warp_sum(acc);
-            }
-        }
-        // mask tokens past the end of the context (their slots may hold anything)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const bool in = (half + 2 * i) < valid;
-#pragma unroll
-            for (int hh = 0; hh < GP; ++hh)
-                s[i][hh] = in ? s[i][hh] : -CUDART_INF_F;
-            if (!in)
-                vr[i] = make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int hh = 0; hh < GP; ++hh) {
-            float mx = s[0][hh];
-#pragma unroll
-            for (int i = 1; i < 8; ++i)
-                mx = fmaxf(mx, s[i][hh]);
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-            const float m_new = fmaxf(m[hh], mx);   // finite: token 0 of a page is always valid
-            const float alpha = ex2_approx(m[hh] - m_new);
-            m[hh] = m_new;
-            float psum = 0.f;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                s[i][hh] = ex2_approx(s[i][hh] - m_new);
-                psum += s[i][hh];
-            }
-            psum += __shfl_xor_sync(0xffffffffu, psum, 16);
-            l[hh] = l[hh] * alpha + psum;
-#pragma unroll
-            for (int d = 0; d < 8; ++d)
-                o[hh][d] *= alpha;
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            float vf[8];
-            unpack8(vr[i], vf);
-#pragma unroll
-            for (int hh = 0; hh < GP; ++hh)
-#pragma unroll
-                for (int d = 0; d < 8; ++d)
-                    o[hh][d] = fmaf(s[i][hh], vf[d], o[hh][d]);
-        }
-    }
-
-    // lanes l and l^16 hold the same head-dim slice for the two token parities
-#pragma unroll
-    for (int hh = 0; hh < GP; ++hh)
-#pragma unroll
-        for (int d = 0; d < 8; ++d)
-            o[hh][d] += __shfl_xor_sync(0xffffffffu, o[hh][d], 16);
-
-    // merge the 4 warps through shared memory
-    __shared__ float sm_o[kDecodeWarps][GP][D];
-    __shared__ float sm_m[kDecodeWarps][GP], sm_l[kDecodeWarps][GP];
-    if (lane < 16) {
-#pragma unroll
-        for (int hh = 0; hh < GP; ++hh)
-#pragma unroll
-            for (int d = 0; d < 8; ++d)
-                sm_o[warp][hh][dofs + d] = o[hh][d];
-    }
-    if (lane == 0) {
-#pragma unroll
-        for (int hh = 0; hh < GP; ++hh) {
-            sm_m[warp][hh] = m[hh];
-            sm_l[warp][hh] = l[hh];
-        }
-    }
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < n_heads * D; idx += blockDim.x) {
-        const int hh = idx / D, d = idx % D;
-        float M = -CUDART_INF_F;
-#pragma unroll
-        for (int w = 0; w < kDecodeWarps; ++w)
-            M = fmaxf(M, sm_m[w][hh]);
-        const size_t row = (size_t)n * H_q + h0 + hh;
-        if (M == -CUDART_INF_F) {
-            // every page of this split had a negative block id (skipped and
-            // flagged above): an empty segment, which the combine step weighs 0
-            O_part[(row * n_split + split) * D + d] = 0.f;
-            if (d == 0)
-                lse_part[row * n_split + split] = -CUDART_INF_F;
-            continue;
-        }
-        float Lsum = 0.f, acc = 0.f;
-#pragma unroll
-        for (int w = 0; w < kDecodeWarps; ++w) {
-            const float c = ex2_approx(sm_m[w][hh] - M);  // 0 for a warp with no pages
-            Lsum += c * sm_l[w][hh];
-            acc += c * sm_o[w][hh][d];
-        }
-        O_part[(row * n_split + split) * D + d] = acc / Lsum;
-        if (d == 0)
-            lse_part[row * n_split + split] = (M + __log2f(Lsum)) * kLn2;
-    }
-}
-
-
 // ---------------------------------------------------------------------------
-// Groups of three or more query heads per kv head: the heads of a group form
-// the 16 rows (zero-padded) of a warp-level tensor-core tile.  Per 16-key page
-// a warp computes S[16 x 16] = Q K^T with 16 m16n8k16 MMAs and O[16 x 128] +=
-// P V with 16 more, so the arithmetic, which outgrows the CUDA cores at ~8
-// FLOP per K/V byte for 8 heads, costs a few hundred cycles per 8 KB page.
-// Pages reach shared memory by 16-byte asynchronous copies into a two-stage
-// ring per warp, rows swizzled (16-byte chunk c of key r at c ^ (r % 8)) so the
-// matrix loads are conflict-free.  Same units, partials and combine as above.
+// The main kernel (the design notes at the top of the file).  Rows of the head
+// tile past the group's heads are computed on zero queries and not written.
 constexpr int kMmaHeads = 16;                       // tile rows: heads per CTA
 constexpr int kMmaStages = 2;                       // pages in flight per warp
 constexpr int kPageBytes = kPageSize * kHeadDim * 2;    // one (page, kv head) of K or V: 4 KB
@@ -754,14 +516,7 @@ lse_combine_rows_kernel(const float* __restrict__ O_part, const float* __restric
 // Rows of at most this many splits are merged one warp per row.
 constexpr int kRowsCombineMaxSplits = 8;
 
-// One or two query heads per kv head: the CUDA-core kernel, all heads of the
-// group in one CTA.  Three or more: the tensor-core kernel's 16-row head tiles.
-int pick_heads_per_cta(int group)
-{
-    if (group <= 2)
-        return group;
-    return kMmaHeads;
-}
+int pick_heads_per_cta(int) { return kMmaHeads; }
 
 // SMs of the current device; a GB300's 152 if it cannot be queried (the
 // workspace size may be asked for on a host without a GPU).
@@ -828,24 +583,6 @@ static void dependent_launch(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr
     cfg.numAttrs = 1;
 }
 
-template <int GP>
-static cudaError_t launch_main(const DecodePlan& p, const void* q, const void* k_cache,
-                               const void* v_cache, const int* block_tables, const int* seq_lens,
-                               float* O_part, float* lse_part, cudaStream_t stream)
-{
-    const long long grid = (long long)p.num_seqs * p.H_kv * p.chunks * p.n_split;
-    if (grid > 0x7fffffffLL)
-        return cudaErrorInvalidConfiguration;
-    const float q_scale = kLog2e / sqrtf((float)kHeadDim);
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    dependent_launch(cfg, attr, dim3((unsigned)grid), dim3(kDecodeWarps * 32), stream);
-    return cudaLaunchKernelEx(&cfg, decode_splitk_kernel<GP>, static_cast<const __half*>(q),
-                              static_cast<const __half*>(k_cache), static_cast<const __half*>(v_cache),
-                              block_tables, seq_lens, O_part, lse_part, p.H_q, p.H_kv, p.group, p.chunks,
-                              p.max_blocks_per_seq, p.pages_per_split, p.n_split, q_scale);
-}
-
 static cudaError_t launch_main_mma(const DecodePlan& p, const void* q, const void* k_cache,
                                    const void* v_cache, const int* block_tables, const int* seq_lens,
                                    float* O_part, float* lse_part, cudaStream_t stream)
@@ -853,16 +590,28 @@ static cudaError_t launch_main_mma(const DecodePlan& p, const void* q, const voi
     const long long grid = (long long)p.num_seqs * p.H_kv * p.chunks * p.n_split;
     if (grid > 0x7fffffffLL)
         return cudaErrorInvalidConfiguration;
-    static bool attr_done[64] = {};
+    // the shared-memory opt-in is a per-context kernel attribute: set once per
+    // device and context (a context that replaced one after a reset gets it too)
+    static std::mutex mtx;
+    static unsigned long long attr_ctx[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
-    if (dev < 64 && !attr_done[dev]) {
-        e = cudaFuncSetAttribute(decode_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmemBytes);
-        if (e != cudaSuccess)
-            return e;
-        attr_done[dev] = true;
+    if (dev < 0 || dev >= 64)
+        return cudaErrorInvalidDevice;
+    unsigned long long ctx = 0;
+    e = current_context_id(&ctx);
+    if (e != cudaSuccess)
+        return e;
+    {
+        std::lock_guard<std::mutex> lock(mtx);
+        if (attr_ctx[dev] != ctx) {
+            e = cudaFuncSetAttribute(decode_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmemBytes);
+            if (e != cudaSuccess)
+                return e;
+            attr_ctx[dev] = ctx;
+        }
     }
     const float scale_log2 = kLog2e / sqrtf((float)kHeadDim);
     cudaLaunchConfig_t cfg = {};
@@ -882,12 +631,7 @@ cudaError_t launch_decode(const DecodePlan& p, const void* q, const void* k_cach
     float* O_part = static_cast<float*>(ws);
     float* lse_part = reinterpret_cast<float*>(static_cast<char*>(ws) +
                                                ((p.o_part_bytes + 255) & ~size_t(255)));
-    cudaError_t e;
-    switch (p.heads_per_cta) {
-    case 1: e = launch_main<1>(p, q, k_cache, v_cache, block_tables, seq_lens, O_part, lse_part, stream); break;
-    case 2: e = launch_main<2>(p, q, k_cache, v_cache, block_tables, seq_lens, O_part, lse_part, stream); break;
-    default: e = launch_main_mma(p, q, k_cache, v_cache, block_tables, seq_lens, O_part, lse_part, stream); break;
-    }
+    cudaError_t e = launch_main_mma(p, q, k_cache, v_cache, block_tables, seq_lens, O_part, lse_part, stream);
     if (e != cudaSuccess)
         return e;
     const int R = p.num_seqs * p.H_q;

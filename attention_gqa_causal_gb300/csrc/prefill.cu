@@ -1066,20 +1066,25 @@ bool make_cache_map(CUtensorMap* m, const void* ptr, long long num_blocks, int H
     return make_map(m, ptr, 4, dims, strides, box);
 }
 
-// the shared-memory opt-in is a per-device, per-kernel attribute
+// the shared-memory opt-in is a per-context, per-kernel attribute: set once per
+// device and context (a context that replaced one after a reset gets it too)
 template <bool PAGED>
 cudaError_t ensure_smem_attr()
 {
     static std::mutex mtx;
-    static bool done[64] = {};
+    static unsigned long long done_ctx[64] = {};   // context the attribute was set in
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
     if (dev < 0 || dev >= 64)
         return cudaErrorInvalidDevice;
+    unsigned long long ctx = 0;
+    e = current_context_id(&ctx);
+    if (e != cudaSuccess)
+        return e;
     std::lock_guard<std::mutex> lock(mtx);
-    if (!done[dev]) {
+    if (done_ctx[dev] != ctx) {
         cudaFuncAttributes fa{};
         e = cudaFuncGetAttributes(&fa, prefill_kernel<PAGED>);
         if (e != cudaSuccess)
@@ -1091,7 +1096,7 @@ cudaError_t ensure_smem_attr()
                                  (int)kSmemAlloc);
         if (e != cudaSuccess)
             return e;
-        done[dev] = true;
+        done_ctx[dev] = ctx;
     }
     return cudaSuccess;
 }

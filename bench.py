@@ -17,7 +17,7 @@ One step is one pass over every hot-path kernel on its workload:
   * the 256-sequence decode step together with its KV append (two launches)
   * paged decode          8 sequences x 32768 tokens, H 16/8
   * paged decode          256 sequences as above, H 64/8 (eight query heads per
-    kv head: the tensor-core decode kernel)
+    kv head in one tensor-core tile)
     (decode: GB/s of K/V bytes of the valid tokens; split-K + combine kernels)
   * the attention-input prologue (QK-norm, RoPE, KV append) of 2 x 8192 new
     tokens, H 32/8 (GB/s of the bytes it must move)
@@ -56,7 +56,6 @@ METRIC = "prefill attn TFLOP/s; paged-decode KV-read GB/s (fraction of GB300 pea
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = {
     "prefill_kernel": ["prefill.cu", "ptx.cuh"],
-    "decode_splitk_kernel": ["decode.cu"],
     "decode_mma_kernel": ["decode.cu"],
     "qk_norm_rope_kernel": ["rope.cu", "ptx.cuh"],
 }
@@ -319,8 +318,6 @@ def build_legs(torch, ag, which):
                                                   inp.block_tables, inp.seq_lens)]
         out = torch.empty_like(t[0])
         leg = Leg(cfg.name, "decode", float(inp.kv_bytes()), "GB/s", 2)
-        # groups of three or more heads per kv head take the tensor-core kernel
-        leg.kernel = "decode_mma_kernel" if cfg.H_q // cfg.H_kv >= 3 else "decode_splitk_kernel"
         leg.set_buffers(lambda t, o: (lambda: ag.attn_decode_paged(t[0], t[1], t[2], o, t[3], t[4])),
                         tuple(t), out)
         leg.host = {"q": inp.q, "k_cache": inp.k_cache, "v_cache": inp.v_cache,
@@ -588,7 +585,7 @@ def run_ours(args):
                                 "traffic": dram_traffic("prefill_kernel", leg.name)}
         else:
             peak = peaks["hbm_gbs"]
-            kernel = "qk_norm_rope_kernel" if leg.kind == "prologue" else getattr(leg, "kernel", "decode_splitk_kernel")
+            kernel = "qk_norm_rope_kernel" if leg.kind == "prologue" else "decode_mma_kernel"
             part["roofline"] = {"bound": "hbm", "achieved": leg.value(ms), "peak": peak,
                                 "unit": "GB/s", "frac": leg.value(ms) / peak,
                                 "peak_kind": f"{peak_src} copy bandwidth",
