@@ -118,7 +118,10 @@ def test_block_relocation_is_bitwise_invariant():
     assert np.array_equal(a, b)
 
 
-@pytest.mark.parametrize("heads", [(8, 8), (16, 8), (12, 4), (32, 8), (16, 2), (10, 2), (16, 1)])
+# groups of 1 to 16 heads fill one tile of 16 head rows; 20 and 32 take two tiles
+# (the second one partly empty for 20)
+@pytest.mark.parametrize("heads", [(8, 8), (16, 8), (12, 4), (32, 8), (16, 2), (10, 2), (16, 1),
+                                   (40, 2), (64, 2)])
 def test_group_sizes(heads):
     H_q, H_kv = heads
     lens = [5, 77, 300, 1024]
