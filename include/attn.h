@@ -160,9 +160,9 @@ ATTN_API int attn_decode_paged(const void* q, const void* k_cache, const void* v
 
 /*
  * Bytes of scratch attn_decode_paged_ws needs for these sizes.
- * pages_per_split: KV pages per split-K work unit.  <= 0 picks the default: 32,
- * halved (down to 4) while the grid would hold fewer than 16 CTAs per SM of
- * the current device (2432 on a 152-SM GB300; 152 SMs are assumed when the
+ * pages_per_split: KV pages per split-K work unit.  <= 0 picks the default: 64,
+ * halved (down to 4) while the grid would hold fewer than 12 CTAs per SM of
+ * the current device (1824 on a 152-SM GB300; 152 SMs are assumed when the
  * device cannot be queried).  Returns 0 for invalid sizes.
  */
 ATTN_API size_t attn_decode_paged_workspace_bytes(int num_seqs, int H_q, int H_kv, int D,

@@ -92,10 +92,10 @@ def test_decode_validation():
 
 def test_workspace_sizes_and_checks():
     ws = ag.attn_decode_paged_workspace_bytes
-    # default split of 32 pages: 128 pages -> 4 splits; [N*H_q*4*128] f32 + [N*H_q*4] f32, 256-aligned
+    # default split of 64 pages: 128 pages -> 2 splits; [N*H_q*2*128] f32 + [N*H_q*2] f32, 256-aligned
     n = ws(256, 16, 8, 128, 128, 16, 0)
-    assert n == 256 * 16 * 4 * 128 * 4 + ((256 * 16 * 4 * 4 + 255) // 256) * 256
-    # a small grid gets smaller splits: 4 seqs x 8 kv heads x ceil(128/pps) CTAs < 2432 down to pps = 4
+    assert n == 256 * 16 * 2 * 128 * 4 + ((256 * 16 * 2 * 4 + 255) // 256) * 256
+    # a small grid gets smaller splits: 4 seqs x 8 kv heads x ceil(128/pps) CTAs < 1824 down to pps = 4
     assert ws(4, 16, 8, 128, 128, 16, 0) == ws(4, 16, 8, 128, 128, 16, 4)
     assert ws(256, 16, 8, 128, 128, 16, 1) == 256 * 16 * 128 * 128 * 4 + 256 * 16 * 128 * 4
     assert ws(8, 16, 8, 128, 2048, 16, 16) == 8 * 16 * 128 * 128 * 4 + ((8 * 16 * 128 * 4 + 255) // 256) * 256

@@ -65,8 +65,8 @@ def test_noalloc_matches_existing_entry_point_and_oracle_on_three_calls():
 
 
 def test_noalloc_refuses_problem_larger_than_its_scratch():
-    # 1024 sequences x 16 heads x 8 splits of partials need ~68 MB > 32 MiB
-    N, H_q, H_kv, mb = 1024, 16, 8, 128
+    # 1024 sequences x 16 heads x 16 splits (of 64 pages) of partials need ~135 MB > 32 MiB
+    N, H_q, H_kv, mb = 1024, 16, 8, 1024
     need = ag.attn_decode_paged_workspace_bytes(N, H_q, H_kv, 128, mb, 16, 0)
     assert need > ag.NOALLOC_SCRATCH_BYTES
     q = torch.zeros(N, H_q, 128, dtype=torch.float16, device="cuda")
