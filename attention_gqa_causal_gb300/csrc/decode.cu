@@ -29,8 +29,10 @@
 //    scores); P is rounded to FP16 for the PV MMA; exp2 uses MUFU ex2.
 //  * The CTA merges its 4 warps in shared memory and writes one partial
 //    (O normalised, lse natural log) per head; the combine kernel merges the
-//    splits.  Empty splits (past the end of a sequence) exit at once and are
-//    skipped by the combine, which recomputes the split count from seq_lens.
+//    splits.  A context that fits one split is finished by the main kernel
+//    (FP16 output, no partial), and the combine leaves its rows alone.  Empty
+//    splits (past the end of a sequence) exit at once and are skipped by the
+//    combine, which recomputes the split count from seq_lens.
 //  * The launches of a step (KV append, main kernel, combine) are chained by
 //    programmatic dependent launch: each kernel lets its dependent be
 //    scheduled as soon as its own CTAs have started, and the dependent waits on
@@ -135,8 +137,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 3)
 decode_mma_kernel(const __half* __restrict__ q, const __half* __restrict__ k_cache,
                   const __half* __restrict__ v_cache, const int* __restrict__ block_tables,
                   const int* __restrict__ seq_lens, float* __restrict__ O_part,
-                  float* __restrict__ lse_part, int H_q, int H_kv, int group, int chunks,
-                  int max_blocks_per_seq, int pages_per_split, int n_split, float scale_log2)
+                  float* __restrict__ lse_part, __half* __restrict__ out, int H_q, int H_kv,
+                  int group, int chunks, int max_blocks_per_seq, int pages_per_split, int n_split,
+                  float scale_log2)
 {
     constexpr int D = kHeadDim;
     constexpr int BS = kPageSize;
@@ -331,8 +334,14 @@ decode_mma_kernel(const __half* __restrict__ q, const __half* __restrict__ k_cac
         for (int w = 0; w < kDecodeWarps; ++w)
             M = fmaxf(M, sm_m[w * kMmaHeads + hh]);
         const size_t row = (size_t)n * H_q + h0 + hh;
+        // a context of one split needs no combine: its output is final here
+        const bool single = n_pages <= pages_per_split;
         if (M == -CUDART_INF_F) {
             // every page of this split had a negative block id: an empty segment
+            if (single) {
+                out[row * D + d] = __float2half_rn(0.f);
+                continue;
+            }
             O_part[(row * n_split + split) * D + d] = 0.f;
             if (d == 0)
                 lse_part[row * n_split + split] = -CUDART_INF_F;
@@ -345,6 +354,10 @@ decode_mma_kernel(const __half* __restrict__ q, const __half* __restrict__ k_cac
             Lsum += c * sm_l[w * kMmaHeads + hh];
             acc += c * sm_o[(w * kMmaHeads + hh) * SO + d];
         }
+        if (single) {
+            out[row * D + d] = __float2half_rn(acc / Lsum);
+            continue;
+        }
         O_part[(row * n_split + split) * D + d] = acc / Lsum;
         if (d == 0)
             lse_part[row * n_split + split] = (M + __log2f(Lsum)) * kLn2;
@@ -355,8 +368,9 @@ decode_mma_kernel(const __half* __restrict__ q, const __half* __restrict__ k_cac
 // head-dim entries.  The warps take the row's splits round-robin (loads
 // unrolled for memory-level parallelism) and are merged in shared memory.
 // If seq_lens is given, row r = n*H_q + h uses the first
-// ceil(ceil(seq_lens[n]/16)/pages_per_split) partials; otherwise all n_split
-// (partials with lse = -inf contribute nothing).
+// ceil(ceil(seq_lens[n]/16)/pages_per_split) partials, and a row of one split
+// is left alone (the main kernel wrote it); otherwise all n_split (partials
+// with lse = -inf contribute nothing).
 constexpr int kCombineWarps = 4;
 
 __global__ void __launch_bounds__(kCombineWarps * 32)
@@ -378,6 +392,8 @@ lse_combine_kernel(const float* __restrict__ O_part, const float* __restrict__ l
         const int L = min(seq_lens[row / H_q], max_len);
         const int pages = (L + kPageSize - 1) / kPageSize;
         ns = (pages + pages_per_split - 1) / pages_per_split;
+        if (ns == 1)
+            return;   // the main kernel wrote this row's output itself
     }
     const float* lp = lse_part + (size_t)row * n_split;
     const float* op = O_part + (size_t)row * n_split * D + lane * 4;
@@ -466,6 +482,8 @@ lse_combine_rows_kernel(const float* __restrict__ O_part, const float* __restric
         const int L = min(seq_lens[row / H_q], max_len);
         const int pages = (L + kPageSize - 1) / kPageSize;
         ns = (pages + pages_per_split - 1) / pages_per_split;
+        if (ns == 1)
+            return;   // the main kernel wrote this row's output itself
     }
     const float* lp = lse_part + (size_t)row * n_split;
     const float* op = O_part + (size_t)row * n_split * D + lane * 4;
@@ -585,8 +603,8 @@ static void dependent_launch(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr
 }
 
 static cudaError_t launch_main_mma(const DecodePlan& p, const void* q, const void* k_cache,
-                                   const void* v_cache, const int* block_tables, const int* seq_lens,
-                                   float* O_part, float* lse_part, cudaStream_t stream)
+                                   const void* v_cache, void* out, const int* block_tables,
+                                   const int* seq_lens, float* O_part, float* lse_part, cudaStream_t stream)
 {
     const long long grid = (long long)p.num_seqs * p.H_kv * p.chunks * p.n_split;
     if (grid > 0x7fffffffLL)
@@ -621,8 +639,9 @@ static cudaError_t launch_main_mma(const DecodePlan& p, const void* q, const voi
     cfg.dynamicSmemBytes = kMmaSmemBytes;
     return cudaLaunchKernelEx(&cfg, decode_mma_kernel, static_cast<const __half*>(q),
                               static_cast<const __half*>(k_cache), static_cast<const __half*>(v_cache),
-                              block_tables, seq_lens, O_part, lse_part, p.H_q, p.H_kv, p.group, p.chunks,
-                              p.max_blocks_per_seq, p.pages_per_split, p.n_split, scale_log2);
+                              block_tables, seq_lens, O_part, lse_part, static_cast<__half*>(out), p.H_q,
+                              p.H_kv, p.group, p.chunks, p.max_blocks_per_seq, p.pages_per_split, p.n_split,
+                              scale_log2);
 }
 
 cudaError_t launch_decode(const DecodePlan& p, const void* q, const void* k_cache,
@@ -632,7 +651,7 @@ cudaError_t launch_decode(const DecodePlan& p, const void* q, const void* k_cach
     float* O_part = static_cast<float*>(ws);
     float* lse_part = reinterpret_cast<float*>(static_cast<char*>(ws) +
                                                ((p.o_part_bytes + 255) & ~size_t(255)));
-    cudaError_t e = launch_main_mma(p, q, k_cache, v_cache, block_tables, seq_lens, O_part, lse_part, stream);
+    cudaError_t e = launch_main_mma(p, q, k_cache, v_cache, out, block_tables, seq_lens, O_part, lse_part, stream);
     if (e != cudaSuccess)
         return e;
     const int R = p.num_seqs * p.H_q;
