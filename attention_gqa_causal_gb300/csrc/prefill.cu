@@ -442,25 +442,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
 
     const bool rope = PAGED && a.rope;
     const int* const trow = PAGED ? a.block_tables + (size_t)w.b * a.max_blocks : nullptr;
-    // one K or V tile into `dst`: a 64 x 128 box per half (contiguous), or
-    // one 64 x 16 box per half and page (paged; a page past the context, or
-    // any id outside the cache, reads as zeros)
+    // one contiguous K or V tile into `dst`: a 64 x 128 box per half (the paged
+    // form copies page by page, in the producer loop below)
     auto load_tile = [&](const CUtensorMap* map, uint32_t dst, uint32_t bar, int j) {
-        if (PAGED) {
-            int phys[kPagesPerTile];
-#pragma unroll
-            for (int k = 0; k < kPagesPerTile; ++k) {
-                const int p = j * kPagesPerTile + k;
-                phys[k] = p < w.n_pages ? trow[p] : -1;
-            }
-#pragma unroll
-            for (int k = 0; k < kPagesPerTile; ++k)
-                for (int h = 0; h < 2; ++h)
-                    tma_load_4d(dst + h * kBoxBytes + k * kPageBoxBytes, map, bar, h * 64, 0, w.g, phys[k]);
-        } else {
-            for (int h = 0; h < 2; ++h)
-                tma_load_4d(dst + h * kBoxBytes, map, bar, h * 64, w.g, j * BN, w.b);
-        }
+        for (int h = 0; h < 2; ++h)
+            tma_load_4d(dst + h * kBoxBytes, map, bar, h * 64, w.g, j * BN, w.b);
     };
     auto load_q = [&](int t, uint32_t bar) {
         for (int h = 0; h < 2; ++h) {
@@ -549,6 +535,26 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 // contiguous: tile 0's K and V went out with the Q tiles
                 int n_k = kEarlyKV && w.n_kv > 0 ? 1 : 0, n_v = n_k;  // K / V tiles issued so far
                 bool ok = true;
+                // paged: a tile is one 64 x 16 box per half and page (a page past
+                // the context, or any id outside the cache, reads as zeros); the page
+                // ids of the next tile are read while this one's stages are awaited,
+                // and serve both its K and its V copies
+                int phys[kPagesPerTile];
+                auto read_pages = [&](int j) {
+#pragma unroll
+                    for (int k = 0; k < kPagesPerTile; ++k) {
+                        const int p = j * kPagesPerTile + k;
+                        phys[k] = p < w.n_pages ? trow[p] : -1;
+                    }
+                };
+                auto load_paged = [&](const CUtensorMap* map, uint32_t dst, uint32_t bar) {
+#pragma unroll
+                    for (int k = 0; k < kPagesPerTile; ++k)
+                        for (int h = 0; h < 2; ++h)
+                            tma_load_4d(dst + h * kBoxBytes + k * kPageBoxBytes, map, bar, h * 64, 0, w.g, phys[k]);
+                };
+                if (PAGED && n_k < w.n_kv)
+                    read_pages(n_k);
                 for (int j = n_k; j < w.n_kv && ok; ++j) {
                     const int sk = j % kKStages;
                     ok = mbar_wait(smem_u32(&ctl.k_empty[sk]), ((j / kKStages) & 1) ^ 1, abort);
@@ -557,7 +563,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     const uint32_t kbar = smem_u32(&ctl.k_full[sk]);
                     if (j != a.stall_tile) {
                         mbar_arrive_expect_tx(kbar, kTileBytes);
-                        load_tile(&tmK, sbase + kSmemK + sk * kTileBytes, kbar, j);
+                        if (PAGED)
+                            load_paged(&tmK, sbase + kSmemK + sk * kTileBytes, kbar);
+                        else
+                            load_tile(&tmK, sbase + kSmemK + sk * kTileBytes, kbar, j);
                     }
                     ++n_k;
                     const int sv = j % kVStages;
@@ -566,7 +575,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                         break;
                     const uint32_t vbar = smem_u32(&ctl.v_full[sv]);
                     mbar_arrive_expect_tx(vbar, kTileBytes);
-                    load_tile(&tmV, sbase + kSmemV + sv * kTileBytes, vbar, j);
+                    if (PAGED) {
+                        load_paged(&tmV, sbase + kSmemV + sv * kTileBytes, vbar);
+                        if (j + 1 < w.n_kv)
+                            read_pages(j + 1);
+                    } else {
+                        load_tile(&tmV, sbase + kSmemV + sv * kTileBytes, vbar, j);
+                    }
                     ++n_v;
                 }
                 if (!ok)
