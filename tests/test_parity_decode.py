@@ -81,7 +81,7 @@ def test_page_decode_cases_identity_table(case):
     assert device_error_clean()
 
 
-@pytest.mark.parametrize("cfg", [W.DECODE_MIX, W.DECODE_LONG], ids=lambda c: c.name)
+@pytest.mark.parametrize("cfg", [W.DECODE_MIX, W.DECODE_LONG, W.DECODE_GQA8], ids=lambda c: c.name)
 def test_decode_workloads_full(cfg):
     inp = W.decode_inputs(cfg, seed=0)
     assert_close(run_decode(inp), oracle_decode(inp), cfg.name)
