@@ -176,9 +176,10 @@ decode_mma_kernel(const __half* __restrict__ q, const __half* __restrict__ k_cac
     // Q as A fragments, rows gid and gid + 8 (zero past the group), 8 K-steps of 16 dims
     uint32_t qa[8][4];
     {
-        const uint32_t* q0 = reinterpret_cast<const uint32_t*>(q + ((size_t)n * H_q + h0 + gid) * D);
-        const uint32_t* q1 = reinterpret_cast<const uint32_t*>(q + ((size_t)n * H_q + h0 + gid + 8) * D);
         const bool v0 = gid < n_heads, v1 = gid + 8 < n_heads;
+        // rows past the group read nothing (their pointers stay on row h0)
+        const uint32_t* q0 = reinterpret_cast<const uint32_t*>(q + ((size_t)n * H_q + h0 + (v0 ? gid : 0)) * D);
+        const uint32_t* q1 = reinterpret_cast<const uint32_t*>(q + ((size_t)n * H_q + h0 + (v1 ? gid + 8 : 0)) * D);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
             qa[kk][0] = v0 ? q0[kk * 8 + tig] : 0u;
